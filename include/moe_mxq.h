@@ -1,0 +1,203 @@
+/*
+ * moe_mxq.h -- C ABI of the MoE expert layer for GB300 (sm_103a).
+ *
+ * The layer (MegaMoE (study notes), "Baseline implementation" and the data-flow
+ * figure after "Combine"; Counting Sort / Bucketization in DeepGEMM Mega MoE,
+ * sections 2 and 5):
+ *
+ *   x bf16 [T,H] --mxq_quantize_act--> xq e4m3 [T,H] + xs ue8m0 [T,H/32]
+ *   logits f32 [T,E] --moe_route_topk--> topk_idx i32 [T,k], topk_w f32 [T,k]
+ *   topk_idx --moe_permute--> counts [E], offsets [E+1], perm [P], inv_perm [P]
+ *   moe_expert_forward: GEMM1 (W1|W3) + SwiGLU (.) topk_w + FP8 requant,
+ *                       GEMM2 (W2) -> y_pairs bf16 [k,T,H]
+ *   moe_combine: y[t] = bf16( sum_j y_pairs[j,t] ) -> y bf16 [T,H]
+ *   moe_forward: all of the above in one call.
+ *
+ * Conventions shared by every entry point
+ *   - Tensor arguments are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or synchronises (except moe_get_device_status,
+ *     which synchronises the given stream).
+ *   - Work is enqueued on the given stream; the return value is a status
+ *     (enum moe_status).  When the host detects an error nothing is enqueued.
+ *   - BF16 is passed as uint16_t bit patterns; FP8 E4M3 codes and UE8M0 scale
+ *     bytes as uint8_t; FP4 E2M1 codes are packed two per byte, the even K
+ *     index in the low nibble.  Indices are int32_t.
+ *   - UE8M0 byte b means 2^(b-127); the scale of a 32-group is
+ *     2^ceil(log2(amax/Q)), Q = 448 (E4M3) or 6 (E2M1), clamped to bytes
+ *     [0,254]; amax = 0 gives byte 0.  Codes round to nearest, ties to even;
+ *     the sign of values that round to zero is kept.
+ *   - Shape limits: K (= H or I) a multiple of 128; 1 <= k <= min(E, 32);
+ *     1 <= E <= 1024; T >= 0 (T = 0 is a no-op); T*k < 2^31.
+ *   - Pointer alignment: 16 bytes for every tensor, 32 bytes for packed FP4
+ *     weights (MOE_ERR_MISALIGNED otherwise).
+ */
+#ifndef MOE_MXQ_H
+#define MOE_MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Same definition as the CUDA runtime's cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *cudaStream_t;
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,         /* null pointer, negative size, bad enum   */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* outside the shape limits above          */
+    MOE_ERR_MISALIGNED = 3,          /* pointer alignment rule broken           */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the stated size   */
+    MOE_ERR_CUDA = 5,                /* a CUDA launch or driver call failed     */
+    MOE_ERR_TIMEOUT = 6,             /* a device-side wait gave up (status word)*/
+    MOE_ERR_DEVICE_INDEX = 7         /* device found an index out of range      */
+};
+
+/* Layouts of quantised weights (mxq_quantize_weight).
+ *
+ * MXQ_LAYOUT_CANONICAL: codes [G][N][K/2] (row n, packed along K),
+ *   scales [G][N][K/32].
+ * MXQ_LAYOUT_MMA_L1 (GEMM1 weights, N = 2I with gate rows [0,I) and up rows
+ *   [I,2I) in the input): rows are interleaved in groups of 8, gate then up
+ *   (MegaMoE (study notes), "_interleave_l1_weights (gran = 8)"): stored row
+ *   r = 16b + c holds input row 8b + c when c < 8 and row I + 8b + c - 8
+ *   otherwise.  Codes are [G][N][K/2] in stored-row order.  Scales are in
+ *   MMA chunk order: [G][N/128][K/128][512], where byte
+ *   (r%32)*16 + (r/32)*4 + kk of chunk (g, nt, kb) is the scale of stored row
+ *   128*nt + r, K-group 4*kb + kk.  N must be a multiple of 128.
+ * MXQ_LAYOUT_MMA_L2 (GEMM2 weights): rows in input order, scales in the same
+ *   chunk order.
+ */
+enum mxq_layout { MXQ_LAYOUT_CANONICAL = 0, MXQ_LAYOUT_MMA_L1 = 1, MXQ_LAYOUT_MMA_L2 = 2 };
+
+/* Activation cast BF16 -> FP8 E4M3 + UE8M0 per 32 along K.
+ * MegaMoE (study notes), "Dispatch" section (per-token cast, gran_k = 32).
+ * x [rows][K] bf16; q [rows][K] e4m3; s [rows][K/32] ue8m0.  rows >= 0. */
+MOE_API int mxq_quantize_act(const uint16_t *x, int64_t rows, int64_t K,
+                     uint8_t *q, uint8_t *s, cudaStream_t stream);
+
+/* Weight cast BF16 [G][N][K] -> FP4 E2M1 packed + UE8M0 per 32 along K, no
+ * grouping along N.  MegaMoE (study notes), "Expert weight quantisation";
+ * the MMA layouts are described at enum mxq_layout.
+ * q: G*N*K/2 bytes; s: G*N*K/32 bytes. */
+MOE_API int mxq_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int64_t K, int layout,
+                        uint8_t *q, uint8_t *s, cudaStream_t stream);
+
+/* Router: per token, the k largest logits (equal logits: lower expert index
+ * first), in descending order, and weights softmax-renormalised over the k
+ * chosen: w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max).
+ * MonoMoe kernel -- design, section 1 (phase 1: softmax top-K, renormalise).
+ * logits [T][E] f32 (finite); topk_idx [T][k] i32; topk_w [T][k] f32. */
+MOE_API int moe_route_topk(const float *logits, int64_t T, int32_t E, int32_t k,
+                   int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+
+/* Counting-sort permute of the P = T*k (token, slot) pairs, pair id
+ * p = t*k + j.  Counting Sort / Bucketization in DeepGEMM Mega MoE,
+ * sections 2.1 (count), 2.2 (prefix sum), 2.3 (scatter), 8.2 (pair id).
+ *   counts[e]  = number of pairs with topk_idx == e             [E]
+ *   offsets[e] = sum of counts[e'] for e' < e; offsets[E] = total [E+1]
+ *   perm[offsets[e] + r] = the r-th smallest pair id routed to e  [P]
+ *                          (stable: token-ascending; entries past offsets[E] untouched)
+ *   inv_perm[p] = position of p in perm, or -1 for a dropped pair  [P]
+ * topk_idx < 0 marks a dropped pair; topk_idx >= E is reported through the
+ * device status word (MOE_ERR_DEVICE_INDEX) of the workspace and the pair is
+ * treated as dropped.  Deterministic: no result depends on thread timing.
+ * workspace: at least moe_permute_workspace_size(T, E, k) bytes, 256-byte
+ * aligned; its status word is reset by the call. */
+MOE_API size_t moe_permute_workspace_size(int64_t T, int32_t E, int32_t k);
+MOE_API int moe_permute(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k,
+                int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Grouped expert GEMMs: GEMM1 (FP8 x FP4 W1|W3, FP32 accumulate) with the
+ * fused epilogue h = silu(gate) * up * topk_w, requantised to E4M3 + UE8M0
+ * per 32 along I; then GEMM2 (FP8 h x FP4 W2) cast to BF16 per pair.
+ * MegaMoE (study notes), "L1 epilogue", "L2 epilogue"; Warp Specialization:
+ * DeepEP vs Mega MoE, epilogue listings.
+ *   xq/xs: activations [T][H] / [T][H/32] (mxq_quantize_act)
+ *   w1q/w1s: GEMM1 weights [E][2I][H] in MXQ_LAYOUT_MMA_L1
+ *   w2q/w2s: GEMM2 weights [E][H][I] in MXQ_LAYOUT_MMA_L2
+ *   topk_idx/topk_w [T][k]; counts/offsets/perm from moe_permute
+ *   y_pairs: output, bf16 [k][T][H]; row (j, t) holds pair p = t*k + j.
+ *            Rows of dropped pairs are not written.
+ *   hq/hs: optional outputs (NULL = not written): the requantised h in pool
+ *          order, hq [P][I] e4m3 and hs [P][I/32] ue8m0, row s = pair perm[s].
+ *   tile_n: token tile (16, 32, 64, 128) or 0 to let the library choose.
+ *   workspace: at least moe_expert_workspace_size(...) bytes, 256-byte aligned.
+ */
+typedef struct moe_expert_args {
+    uint32_t struct_size;   /* sizeof(moe_expert_args) */
+    int64_t T, H, I;
+    int32_t E, k;
+    const uint8_t *xq, *xs;
+    const uint8_t *w1q, *w1s, *w2q, *w2s;
+    const int32_t *topk_idx;
+    const float *topk_w;
+    const int32_t *counts, *offsets, *perm;
+    uint16_t *y_pairs;
+    uint8_t *hq, *hs;
+    int32_t tile_n;
+    void *workspace;
+    size_t workspace_bytes;
+} moe_expert_args;
+
+MOE_API size_t moe_expert_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k);
+MOE_API int moe_expert_forward(const moe_expert_args *args, cudaStream_t stream);
+
+/* Top-k combine: y[t][n] = bf16( sum over slots j with topk_idx[t][j] >= 0 of
+ * y_pairs[j][t][n] ), summed in FP32 in slot order.  The top-k weight was
+ * applied before GEMM2, so the sum is unweighted.  MegaMoE (study notes),
+ * "Combine" and "L2 epilogue"; Warp Specialization: DeepEP vs Mega MoE,
+ * combine listing.  y_pairs [k][T][H]; y [T][H]. */
+MOE_API int moe_combine(const uint16_t *y_pairs, const int32_t *topk_idx, int64_t T, int32_t k,
+                int64_t H, uint16_t *y, cudaStream_t stream);
+
+/* The whole layer in one call (quantise, route, permute, GEMM1+epilogue,
+ * GEMM2, combine).  Inputs: x bf16 [T][H], logits f32 [T][E], weights as for
+ * moe_expert_forward.  Output y bf16 [T][H].  Optional outputs (NULL = not
+ * written): topk_idx/topk_w [T][k], counts [E], offsets [E+1], perm [P].
+ * workspace: at least moe_workspace_size(T, H, I, E, k) bytes, 256-byte
+ * aligned; the call resets what it needs, callers do not zero it. */
+typedef struct moe_forward_args {
+    uint32_t struct_size;   /* sizeof(moe_forward_args) */
+    int64_t T, H, I;
+    int32_t E, k;
+    const uint16_t *x;
+    const float *logits;
+    const uint8_t *w1q, *w1s, *w2q, *w2s;
+    uint16_t *y;
+    int32_t *topk_idx_out;
+    float *topk_w_out;
+    int32_t *counts_out, *offsets_out, *perm_out;
+    int32_t tile_n;
+    void *workspace;
+    size_t workspace_bytes;
+} moe_forward_args;
+
+MOE_API size_t moe_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k);
+MOE_API int moe_forward(const moe_forward_args *args, cudaStream_t stream);
+
+/* Reads the device status word that kernels write into a workspace (first
+ * 4 bytes of any workspace above): MOE_OK, MOE_ERR_TIMEOUT (a bounded
+ * device-side wait gave up) or MOE_ERR_DEVICE_INDEX.  Synchronises `stream`. */
+MOE_API int moe_get_device_status(const void *workspace, cudaStream_t stream, int *out);
+
+/* Human-readable text of a status code (static storage). */
+MOE_API const char *moe_status_string(int status);
+
+/* Library version string (static storage). */
+MOE_API const char *moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_MXQ_H */

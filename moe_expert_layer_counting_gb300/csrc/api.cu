@@ -1,0 +1,182 @@
+// api.cu -- the fused entry point moe_forward, workspace sizing, status
+// helpers and the host utilities (SM count, tensor-map encoding) used by the
+// other translation units.
+//
+// moe_forward enqueues, on one stream: activation cast (mxq_quantize_act),
+// routing (moe_route_topk), the counting-sort permute (moe_permute), the two
+// grouped GEMMs (moe_expert_forward) and the combine (moe_combine) -- the
+// order of the MegaMoE baseline pipeline (MegaMoE (study notes), "Baseline
+// implementation"), with dispatch and combine as local gather/scatter in HBM.
+// The workspace sizing mirrors the MonoMoe scratchpad discipline (MonoMoe
+// kernel -- design, section 4): one caller-provided buffer whose size the
+// library reports, and whatever must start at zero is reset inside the call.
+#include <cstdio>
+#include <mutex>
+
+#include "host_common.h"
+
+namespace mxq {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint64_t dim0, uint64_t dim1,
+                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+struct ForwardWs {
+  size_t xq, xs, idx, w, counts, offsets, perm, inv_perm, perm_scratch, expert, y_pairs, total;
+};
+
+ForwardWs forward_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  const int64_t P = T * k;
+  ForwardWs w;
+  size_t off = kStatusBytes;
+  w.xq = off;           off += round_up((size_t)T * H, 256);
+  w.xs = off;           off += round_up((size_t)T * (H / 32), 256);
+  w.idx = off;          off += round_up((size_t)P * 4, 256);
+  w.w = off;            off += round_up((size_t)P * 4, 256);
+  w.counts = off;       off += round_up((size_t)E * 4, 256);
+  w.offsets = off;      off += round_up((size_t)(E + 1) * 4, 256);
+  w.perm = off;         off += round_up((size_t)P * 4, 256);
+  w.inv_perm = off;     off += round_up((size_t)P * 4, 256);
+  w.perm_scratch = off; off += permute_scratch_bytes(T, (int)E, (int)k);
+  w.expert = off;       off += expert_ws_layout(T, H, I, E, k).total;
+  w.y_pairs = off;      off += round_up((size_t)P * H * 2, 256);
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+}  // namespace mxq
+
+using namespace mxq;
+
+extern "C" size_t moe_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return 0;
+  return forward_ws_layout(T, H, I, E, k).total;
+}
+
+extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
+  if (!a || a->struct_size != sizeof(moe_forward_args)) return MOE_ERR_INVALID_ARG;
+  if (a->T < 0 || a->H <= 0 || a->I <= 0 || a->E <= 0 || a->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (!a->workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a->workspace, 256)) return MOE_ERR_MISALIGNED;
+  const ForwardWs lay = forward_ws_layout(a->T, a->H, a->I, a->E, a->k);
+  if (a->workspace_bytes < lay.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  char *ws = reinterpret_cast<char *>(a->workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  const int64_t P = a->T * a->k;
+
+  moe_expert_args ea{};
+  ea.struct_size = sizeof(moe_expert_args);
+  ea.T = a->T; ea.H = a->H; ea.I = a->I; ea.E = a->E; ea.k = a->k;
+  ea.xq = reinterpret_cast<uint8_t *>(ws + lay.xq);
+  ea.xs = reinterpret_cast<uint8_t *>(ws + lay.xs);
+  ea.w1q = a->w1q; ea.w1s = a->w1s; ea.w2q = a->w2q; ea.w2s = a->w2s;
+  int32_t *idx = a->topk_idx_out ? a->topk_idx_out : reinterpret_cast<int32_t *>(ws + lay.idx);
+  float *wts = a->topk_w_out ? a->topk_w_out : reinterpret_cast<float *>(ws + lay.w);
+  int32_t *counts = a->counts_out ? a->counts_out : reinterpret_cast<int32_t *>(ws + lay.counts);
+  int32_t *offsets = a->offsets_out ? a->offsets_out : reinterpret_cast<int32_t *>(ws + lay.offsets);
+  int32_t *perm = a->perm_out ? a->perm_out : reinterpret_cast<int32_t *>(ws + lay.perm);
+  ea.topk_idx = idx; ea.topk_w = wts; ea.counts = counts; ea.offsets = offsets; ea.perm = perm;
+  ea.y_pairs = reinterpret_cast<uint16_t *>(ws + lay.y_pairs);
+  ea.tile_n = a->tile_n;
+  ea.workspace = ws + lay.expert;              // not used for sizing checks below
+  ea.workspace_bytes = 0;
+  int rc = check_expert_args(&ea, false);
+  if (rc != MOE_OK) return rc;
+  if (a->T > 0) {
+    if (!a->x || !a->logits || !a->y) return MOE_ERR_INVALID_ARG;
+    if (!aligned(a->x, 16) || !aligned(a->logits, 16) || !aligned(a->y, 16)) return MOE_ERR_MISALIGNED;
+    if ((a->topk_idx_out && !aligned(a->topk_idx_out, 16)) || (a->topk_w_out && !aligned(a->topk_w_out, 16)))
+      return MOE_ERR_MISALIGNED;
+  }
+
+  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (a->T == 0) {
+    if (a->counts_out && cudaMemsetAsync(a->counts_out, 0, (size_t)a->E * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (a->offsets_out && cudaMemsetAsync(a->offsets_out, 0, (size_t)(a->E + 1) * 4, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  rc = launch_quant_act(a->x, a->T, a->H, const_cast<uint8_t *>(ea.xq), const_cast<uint8_t *>(ea.xs), st);
+  if (rc != MOE_OK) return rc;
+  rc = launch_route(a->logits, a->T, a->E, a->k, idx, wts, st);
+  if (rc != MOE_OK) return rc;
+  rc = launch_permute(idx, a->T, a->E, a->k, counts, offsets, perm, reinterpret_cast<int32_t *>(ws + lay.inv_perm),
+                      status, ws + lay.perm_scratch, st);
+  if (rc != MOE_OK) return rc;
+  rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
+  if (rc != MOE_OK) return rc;
+  (void)P;
+  return launch_combine(ea.y_pairs, idx, a->T, a->k, a->H, a->y, st);
+}
+
+extern "C" int moe_get_device_status(const void *workspace, cudaStream_t stream, int *out) {
+  if (!workspace || !out) return MOE_ERR_INVALID_ARG;
+  int host = 0;
+  if (cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  *out = host;
+  return MOE_OK;
+}
+
+extern "C" const char *moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad enum)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (see the shape limits in moe_mxq.h)";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer (16 bytes; 32 for packed FP4 weights)";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than the reported size";
+    case MOE_ERR_CUDA: return "CUDA launch or driver call failed";
+    case MOE_ERR_TIMEOUT: return "a device-side wait gave up (timeout)";
+    case MOE_ERR_DEVICE_INDEX: return "device found an expert index out of range";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char *moe_version(void) { return "moe_mxq 0.1 (sm_103a, tcgen05 block-scaled)"; }

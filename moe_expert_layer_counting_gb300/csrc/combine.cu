@@ -1,0 +1,74 @@
+// combine.cu -- top-k combine back to token order.
+//
+// MegaMoE (study notes), "Combine" and "L2 epilogue"; Warp Specialization:
+// DeepEP vs Mega MoE, combine listing: the k BF16 copies of a token are
+// summed in FP32 and cast to BF16 once.  The top-k weight already scaled h
+// before GEMM2, so the sum is unweighted.  Dropped slots (index < 0) are
+// skipped.  One thread owns 8 output values (16-byte loads and stores);
+// the slot sum runs in slot order, so the result is deterministic.
+#include <cuda_bf16.h>
+
+#include "host_common.h"
+#include "ptx.cuh"
+
+namespace mxq {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(const uint4 *__restrict__ yp,
+                                                           const int32_t *__restrict__ idx, int64_t T, int k,
+                                                           int64_t H8, uint4 *__restrict__ y) {
+  const int64_t items = T * H8;
+  const int64_t slot_stride = T * H8;        // uint4 elements between slots
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / H8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      if (__ldg(idx + t * k + j) < 0) continue;
+      const uint4 v = __ldg(yp + j * slot_stride + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += bf16_bits_to_float(w[q] & 0xFFFFu);
+        acc[2 * q + 1] += bf16_bits_to_float(w[q] >> 16);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      o[q] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    y[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace
+
+int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k, int64_t H, uint16_t *y,
+                   cudaStream_t st) {
+  if (T == 0) return MOE_OK;
+  const int64_t items = T * (H / 8);
+  const int64_t blocks = ceil_div(items, kThreads);
+  const int64_t cap = (int64_t)num_sms() * 8;
+  combine_kernel<<<(int)(blocks < cap ? blocks : cap), kThreads, 0, st>>>(
+      reinterpret_cast<const uint4 *>(y_pairs), idx, T, k, H / 8, reinterpret_cast<uint4 *>(y));
+  return launch_status();
+}
+
+}  // namespace mxq
+
+using namespace mxq;
+
+extern "C" int moe_combine(const uint16_t *y_pairs, const int32_t *topk_idx, int64_t T, int32_t k, int64_t H,
+                           uint16_t *y, cudaStream_t stream) {
+  if (T < 0 || k <= 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+  if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!y_pairs || !topk_idx || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_pairs, 16) || !aligned(y, 16)) return MOE_ERR_MISALIGNED;
+  return launch_combine(y_pairs, topk_idx, T, k, H, y, stream);
+}

@@ -1,0 +1,554 @@
+// gemm.cu -- grouped expert GEMMs on tcgen05 block-scaled MMA (sm_103a).
+//
+// GEMM1 (W1|W3, FP8 E4M3 tokens x FP4 E2M1 weights, UE8M0 per 32 along K,
+// FP32 accumulate in TMEM) with the fused epilogue
+//     h = silu(gate) * up * topk_w  ->  E4M3 + UE8M0 per 32 along I,
+// then GEMM2 (FP8 h x FP4 W2) with a BF16 epilogue that scatters each pair's
+// row to y_pairs[slot][token].
+//
+// Prior art: MegaMoE (study notes), "Warp roles", "Scheduler", "L1
+// epilogue", "L2 epilogue" and the gate/up interleave; Warp Specialization:
+// DeepEP vs Mega MoE (MMA issue with the weights in the M slot, UTCCP copy of
+// the scale factors into TMEM, epilogue listings).  What is kept on sm_103a:
+//   * weights are the MMA's M operand (128 rows per tile) and tokens the N
+//     operand (16..128 per tile), so decode-sized experts waste little MMA;
+//   * one persistent CTA per SM, warp roles: warp 0 TMA producer, warp 1
+//     TMEM allocator + single-thread MMA issuer, warps 2-5 epilogue (one TMEM
+//     lane quadrant each);
+//   * a ring of shared-memory stages (full/empty mbarriers) and two TMEM
+//     accumulators (tmem_full/tmem_empty) so loads, MMAs and the epilogue of
+//     consecutive tiles overlap;
+//   * FP4 weights are unpacked into 8-bit containers by TMA
+//     (16U4_ALIGN16B, 128B swizzle); token rows of GEMM1 are gathered from
+//     the un-permuted FP8 activations with TMA tile::gather4 by pair id,
+//     which replaces the pages' NVLink pull into a pool buffer;
+//   * scale factors travel as 512-byte chunks already in the tcgen05.cp
+//     32x128b.warpx4 order and land in TMEM next to the accumulators.
+// Not kept: the dispatch warps and NVLink stores (one GPU), the 2-SM
+// cluster, and unbounded spins (every wait here gives up after ~1 s and
+// reports MOE_ERR_TIMEOUT through the workspace status word).
+//
+// Work order (all roles walk the same list): expert-major, then weight tile
+// mt, then token tile nt, so consecutive CTAs share a weight tile (token
+// tiles of one expert) or a token tile (weight tiles of one expert) in L2.
+#include <cuda_bf16.h>
+
+#include "host_common.h"
+#include "ptx.cuh"
+
+namespace mxq {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 128;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kChunk = 16;                    // accumulator columns per epilogue step
+constexpr long long kWaitLimit = 2000000000LL;
+constexpr int kMaxE = 1024;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kABytes = kBM * kBK;                 // unpacked FP4 (8-bit containers)
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kSfbBytes = (BN < 32 ? BN : 32) * 16;
+  static constexpr int kStageBytes = kABytes + kBBytes + 1024;
+  static constexpr int kStages = (200 * 1024 / kStageBytes) > 12 ? 12 : (200 * 1024 / kStageBytes);
+  static constexpr int kTmemCols = 2 * BN + 8 * kStages;
+  static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
+                                         : kTmemCols <= 256 ? 256 : 512;
+  static constexpr uint32_t kTxBytes = kABytes + kBBytes + 512 + kSfbBytes;
+  // shared memory carve-up (offsets from a 1024-aligned base)
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffSfa = kOffB + kStages * kBBytes;
+  static constexpr int kOffSfb = kOffSfa + kStages * 512;
+  static constexpr int kOffEpi = kOffSfb + kStages * 512;   // 4 KB epilogue staging
+  static constexpr int kOffRow = kOffEpi + 4096;            // pair id [BN] + weight [BN]
+  static constexpr int kOffBar = kOffRow + 8 * BN;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
+  static constexpr int kOffExp = kOffTmemPtr + 32;          // tile_off, counts, offsets: 3*(E+1) ints
+  static_assert(kStages >= 2, "need at least two stages");
+};
+
+template <int BN>
+size_t smem_bytes(int E) {
+  return 1024 + Cfg<BN>::kOffExp + (size_t)3 * (E + 1) * 4;
+}
+
+struct GemmArgs {
+  int E, k, T, H, I;
+  int M, K, KB, MT;                 // weight rows / reduction / K blocks / weight tiles per expert
+  const int32_t *counts, *offsets, *perm;
+  const float *topk_w;
+  const uint8_t *w_sf;              // [E][MT][KB][512]
+  const uint8_t *b_sf;              // [tiles][KB][512]
+  uint8_t *hq;                      // L1 out [P][I] (pool order)
+  uint8_t *sfb2;                    // L1 out [tiles][I/128][512]
+  uint8_t *hs_out;                  // optional L1 out [P][I/32]
+  uint16_t *y_pairs;                // L2 out [k][T][H]
+  int *status;
+};
+
+struct TileInfo {
+  int e, mt, g, s0, valid;
+};
+
+// Exclusive prefix of ceil(counts[e] / BN) computed by one warp into
+// tile_off[0..E]; also copies counts and offsets to shared memory.
+template <int BN>
+__device__ void build_tile_map(const int32_t *counts, const int32_t *offsets, int E, int *tile_off, int *cnt_sm,
+                               int *off_sm) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  for (int b = 0; b < E; b += 32) {
+    const int e = b + lane;
+    const int c = e < E ? __ldg(counts + e) : 0;
+    const int nt = (c + BN - 1) / BN;
+    int inc = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += n;
+    }
+    if (e < E) {
+      tile_off[e] = carry + inc - nt;
+      cnt_sm[e] = c;
+      off_sm[e] = __ldg(offsets + e);
+    }
+    carry += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) {
+    tile_off[E] = carry;
+    off_sm[E] = __ldg(offsets + E);
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int *tile_off, const int *cnt_sm,
+                                                const int *off_sm) {
+  const int tq = w / MT;
+  int lo = 0, hi = E;                // find e with tile_off[e] <= tq < tile_off[e+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_off[mid] <= tq) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.e = lo;
+  const int nte = tile_off[lo + 1] - tile_off[lo];
+  const int local = w - tile_off[lo] * MT;
+  ti.mt = local / nte;
+  const int nt = local - ti.mt * nte;
+  ti.g = tile_off[lo] + nt;
+  ti.s0 = off_sm[lo] + nt * BN;
+  const int rem = cnt_sm[lo] - nt * BN;
+  ti.valid = rem < BN ? rem : BN;
+  return ti;
+}
+
+template <int BN, int PHASE>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
+                       const GemmArgs args) {
+  using C = Cfg<BN>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+  uint64_t *full = bars;
+  uint64_t *empty = bars + C::kStages;
+  uint64_t *tmem_full = bars + 2 * C::kStages;
+  uint64_t *tmem_empty = tmem_full + 2;
+  uint64_t *mma_done = tmem_full + 4;
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::kOffTmemPtr);
+  int *tile_off = reinterpret_cast<int *>(smem + C::kOffExp);
+  int *cnt_sm = tile_off + (args.E + 1);
+  int *off_sm = cnt_sm + (args.E + 1);
+  int32_t *row_pair = reinterpret_cast<int32_t *>(smem + C::kOffRow);
+  float *row_w = reinterpret_cast<float *>(smem + C::kOffRow + 4 * BN);
+  int *vote = reinterpret_cast<int *>(smem + C::kOffTmemPtr + 4);     // [4], one per epilogue warp
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int *status = args.status;
+
+  if (warp == 0) {
+    build_tile_map<BN>(args.counts, args.offsets, args.E, tile_off, cnt_sm, off_sm);
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_w);
+      tma_prefetch_desc(&tmap_b);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      for (int a = 0; a < 2; ++a) {
+        mbar_init(&tmem_full[a], 1);
+        mbar_init(&tmem_empty[a], kEpiThreads / 32);
+      }
+      mbar_init(mma_done, 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    tmem_alloc(tmem_ptr, C::kTmemAlloc);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_ptr;
+  const int total_work = tile_off[args.E] * args.MT;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, issued_phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+      const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      int tok[4] = {0, 0, 0, 0};
+      if (PHASE == 1 && lane < BN / 4) {
+        const int first = __ldg(args.perm + ti.s0) / args.k;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane * 4 + i;
+          tok[i] = r < ti.valid ? __ldg(args.perm + ti.s0 + r) / args.k : first;
+        }
+      }
+      const int wrow = ti.e * args.M + ti.mt * kBM;
+      const uint8_t *sfa_src = args.w_sf + ((size_t)(ti.e * args.MT + ti.mt) * args.KB) * 512;
+      const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB) * 512;
+      for (int kb = 0; kb < args.KB; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit))) {
+          ok = false;
+          break;
+        }
+        unsigned char *a_dst = smem + C::kOffA + stage * C::kABytes;
+        unsigned char *b_dst = smem + C::kOffB + stage * C::kBBytes;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], C::kTxBytes);
+          tma_load_2d(a_dst, &tmap_w, &full[stage], kb * kBK, wrow);
+          bulk_load(smem + C::kOffSfa + stage * 512, sfa_src + (size_t)kb * 512, 512, &full[stage]);
+          bulk_load(smem + C::kOffSfb + stage * 512, sfb_src + (size_t)kb * 512, C::kSfbBytes, &full[stage]);
+          if (PHASE == 2) tma_load_2d(b_dst, &tmap_b, &full[stage], kb * kBK, ti.s0);
+        }
+        __syncwarp();
+        if (PHASE == 1 && lane < BN / 4)
+          tma_gather4(b_dst + lane * 4 * kBK, &tmap_b, &full[stage], kb * kBK, tok[0], tok[1], tok[2], tok[3]);
+        issued_mask |= 1u << stage;
+        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+    // never leave with copies in flight: wait for the last load of each stage
+    for (int s = 0; s < C::kStages; ++s)
+      if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&tmem_empty[acc], acc_phase ^ 1, status, kWaitLimit))) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < args.KB; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, status, kWaitLimit))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + 8 * stage);
+          const uint32_t sfa = smem_u32(smem + C::kOffSfa + stage * 512);
+          const uint32_t sfb = smem_u32(smem + C::kOffSfb + stage * 512);
+          tc_cp_32x128b_warpx4(sf_col, make_smem_desc(sfa, 0, 128, kSwizzleNone));
+          tc_cp_32x128b_warpx4(sf_col + 4, make_smem_desc(sfb, 0, 128, kSwizzleNone));
+          const uint32_t a_base = smem_u32(smem + C::kOffA + stage * C::kABytes);
+          const uint32_t b_base = smem_u32(smem + C::kOffB + stage * C::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = make_smem_desc(a_base + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = make_smem_desc(b_base + kk * 32, 16, 1024, kSwizzle128B);
+            tc_mma_mxf8f6f4(d_tmem, ad, bd, make_idesc_fp4w_fp8a(BN, kk), sf_col, sf_col + 4,
+                            (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&tmem_full[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    // all MMAs issued by this thread complete before TMEM is released
+    if (lane == 0) tc_commit(mma_done);
+    __syncwarp();
+    mbar_wait(mma_done, 0, status, kWaitLimit);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lane quadrant of this warp
+    const int et = threadIdx.x - 64;         // 0..127
+    float *ebuf_f = reinterpret_cast<float *>(smem + C::kOffEpi);
+    uint16_t *ebuf_h = reinterpret_cast<uint16_t *>(smem + C::kOffEpi);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
+      const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      if (et < BN) {
+        int p = -1;
+        float wt = 0.f;
+        if (et < ti.valid) {
+          p = __ldg(args.perm + ti.s0 + et);
+          if (PHASE == 1) wt = __ldg(args.topk_w + p);
+        }
+        row_pair[et] = p;
+        row_w[et] = wt;
+      }
+      // the four epilogue warps agree on the outcome of the bounded wait before
+      // any of them enters another named barrier
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&tmem_full[acc], acc_phase, status, kWaitLimit));
+      if (lane == 0) vote[q] = got ? 1 : 0;
+      named_bar_sync(1, kEpiThreads);
+      if (!(vote[0] & vote[1] & vote[2] & vote[3])) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      for (int c0 = 0; c0 < BN; c0 += kChunk) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(t_row + (uint32_t)c0, v);
+        tmem_ld_wait();
+        if (PHASE == 1) {
+          // lane l of quadrant q holds stored row 32q+l: gate when (l & 8) == 0,
+          // the matching up row sits 8 lanes away (8-row gate/up interleave).
+          const bool is_gate = (lane & 8) == 0;
+          const int feat = 16 * q + 8 * (lane >> 4) + (lane & 7);   // tile-local feature 0..63
+          const int jbase = is_gate ? 0 : 8;                         // columns this lane evaluates
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float mine = __uint_as_float(v[j]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
+            if (j >= jbase && j < jbase + 8) {
+              const float g = is_gate ? mine : other;
+              const float u = is_gate ? other : mine;
+              const float h = g / (1.0f + __expf(-g)) * u * row_w[c0 + j];
+              ebuf_f[j * 64 + feat] = h;
+            }
+          }
+          named_bar_sync(1, kEpiThreads);
+          // requantise: 16 columns x 2 groups of 32 features, 8 items per warp
+#pragma unroll 1
+          for (int it = q; it < 2 * kChunk; it += 4) {
+            const int col = it >> 1, grp = it & 1;
+            const float h = ebuf_f[col * 64 + grp * 32 + lane];
+            const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
+            const int e = ue8m0_exponent<true>(__uint_as_float(amax_bits));
+            const uint8_t code = (uint8_t)(cvt_e4m3x2(h * pow2_neg(e), 0.f) & 0xFFu);
+            const int c = c0 + col;
+            if (c < ti.valid) {
+              const size_t s = (size_t)(ti.s0 + c);
+              const int fcol = ti.mt * 64 + grp * 32;                // first feature of the group
+              args.hq[s * args.I + fcol + lane] = code;
+              if (lane == 0) {
+                const int fg = fcol >> 5;                             // 32-group index along I
+                const size_t chunk = (size_t)ti.g * (args.I / 128) + (fg >> 2);
+                args.sfb2[chunk * 512 + (c & 31) * 16 + (c >> 5) * 4 + (fg & 3)] = (uint8_t)(e + 127);
+                if (args.hs_out) args.hs_out[s * (args.I / 32) + fg] = (uint8_t)(e + 127);
+              }
+            }
+          }
+          named_bar_sync(1, kEpiThreads);
+        } else {
+          const int row = 32 * q + lane;                             // output feature inside the tile
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
+            ebuf_h[j * 128 + row] = *reinterpret_cast<const uint16_t *>(&b);
+          }
+          named_bar_sync(1, kEpiThreads);
+#pragma unroll
+          for (int it = 0; it < 2; ++it) {
+            const int col = q + 4 * (2 * it + (lane >> 4));
+            const int c = c0 + col;
+            if (c < ti.valid) {
+              const int p = row_pair[c];
+              const int t = p / args.k, j = p - t * args.k;
+              const int l16 = lane & 15;
+              uint16_t *dst = args.y_pairs + ((size_t)j * args.T + t) * args.H + (size_t)ti.mt * kBM + l16 * 8;
+              *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(ebuf_h + col * 128 + l16 * 8);
+            }
+          }
+          named_bar_sync(1, kEpiThreads);
+        }
+      }
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemAlloc);
+  }
+}
+
+// Token-scale chunks of GEMM1: for pool row s (tile g, row r) copy the 4
+// scale bytes of K block kb of token perm[s]/k into chunk (g, kb) at byte
+// (r%32)*16 + (r/32)*4.
+template <int BN>
+__global__ void __launch_bounds__(256) prep_sfb1_kernel(const uint8_t *__restrict__ xs,
+                                                        const int32_t *__restrict__ counts,
+                                                        const int32_t *__restrict__ offsets,
+                                                        const int32_t *__restrict__ perm, int E, int k, int KB,
+                                                        uint8_t *__restrict__ sfb1) {
+  extern __shared__ int sh[];
+  int *tile_off = sh, *cnt_sm = sh + (E + 1), *off_sm = sh + 2 * (E + 1);
+  if (threadIdx.x < 32) build_tile_map<BN>(counts, offsets, E, tile_off, cnt_sm, off_sm);
+  __syncthreads();
+  const int P = off_sm[E];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  for (int s = blockIdx.x * nwarps + warp; s < P; s += gridDim.x * nwarps) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off_sm[mid] <= s) lo = mid; else hi = mid;
+    }
+    // skip empty experts that share the same offset
+    while (lo + 1 < E && off_sm[lo + 1] <= s) ++lo;
+    const int rank = s - off_sm[lo];
+    const int g = tile_off[lo] + rank / BN, r = rank % BN;
+    const int t = __ldg(perm + s) / k;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(xs + (size_t)t * KB * 4);
+    for (int kb = lane; kb < KB; kb += 32) {
+      const uint32_t wv = __ldg(src + kb);
+      *reinterpret_cast<uint32_t *>(sfb1 + ((size_t)g * KB + kb) * 512 + (r & 31) * 16 + (r >> 5) * 4) = wv;
+    }
+  }
+}
+
+template <int BN>
+int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &lay, cudaStream_t st) {
+  uint8_t *sfb1 = reinterpret_cast<uint8_t *>(ws + lay.sfb1);
+  uint8_t *sfb2 = reinterpret_cast<uint8_t *>(ws + lay.sfb2);
+  uint8_t *hq = a->hq ? a->hq : reinterpret_cast<uint8_t *>(ws + lay.hq);
+  const int64_t P = a->T * a->k;
+  const int E = a->E;
+
+  // 1. token-scale chunks for GEMM1
+  {
+    const size_t sm = (size_t)3 * (E + 1) * 4;
+    const int64_t blocks = ceil_div(P, 8);
+    const int grid = (int)(blocks < num_sms() * 4 ? (blocks > 0 ? blocks : 1) : num_sms() * 4);
+    prep_sfb1_kernel<BN><<<grid, 256, sm, st>>>(a->xs, a->counts, a->offsets, a->perm, E, a->k, (int)(a->H / 128),
+                                                 sfb1);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  }
+
+  // 2. tensor maps
+  CUtensorMap tw1, tx, tw2, th;
+  bool ok = encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, (uint64_t)a->H,
+                           (uint64_t)E * 2 * a->I, (uint64_t)a->H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a->xq, (uint64_t)a->H, (uint64_t)a->T,
+                            (uint64_t)a->H, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, (uint64_t)a->I,
+                            (uint64_t)E * a->H, (uint64_t)a->I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
+                            (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return MOE_ERR_CUDA;
+
+  GemmArgs g{};
+  g.E = E; g.k = a->k; g.T = (int)a->T; g.H = (int)a->H; g.I = (int)a->I;
+  g.counts = a->counts; g.offsets = a->offsets; g.perm = a->perm; g.topk_w = a->topk_w;
+  g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
+
+  const size_t sm = smem_bytes<BN>(E);
+  const int grid = num_sms();
+  // 3. GEMM1 + SwiGLU (.) weight + FP8 requantisation
+  g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
+  g.w_sf = a->w1s; g.b_sf = sfb1;
+  if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  expert_gemm_kernel<BN, 1><<<grid, kThreads, sm, st>>>(tw1, tx, g);
+  if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  // 4. GEMM2 -> BF16 per pair
+  g.M = (int)a->H; g.K = (int)a->I; g.KB = (int)(a->I / 128); g.MT = (int)(a->H / 128);
+  g.w_sf = a->w2s; g.b_sf = sfb2;
+  if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  expert_gemm_kernel<BN, 2><<<grid, kThreads, sm, st>>>(tw2, th, g);
+  return launch_status();
+}
+
+}  // namespace
+
+int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, cudaStream_t st) {
+  const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
+  if (a->T == 0) return MOE_OK;
+  char *ws = reinterpret_cast<char *>(scratch);
+  const int bn = a->tile_n ? a->tile_n : choose_tile_n(a->T * a->k, a->E);
+  switch (bn) {
+    case 16: return run_expert<16>(a, status, ws, lay, st);
+    case 32: return run_expert<32>(a, status, ws, lay, st);
+    case 64: return run_expert<64>(a, status, ws, lay, st);
+    case 128: return run_expert<128>(a, status, ws, lay, st);
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
+int check_expert_args(const moe_expert_args *a, bool need_ws) {
+  if (!a) return MOE_ERR_INVALID_ARG;
+  if (a->struct_size != sizeof(moe_expert_args)) return MOE_ERR_INVALID_ARG;
+  if (a->T < 0 || a->H <= 0 || a->I <= 0 || a->E <= 0 || a->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (a->H % 128 || a->I % 128 || a->E > kMaxE || a->k > a->E || a->k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (a->T * (int64_t)a->k >= ((int64_t)1 << 31) || a->H * a->E >= ((int64_t)1 << 31) ||
+      2 * a->I * a->E >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (a->tile_n != 0 && a->tile_n != 16 && a->tile_n != 32 && a->tile_n != 64 && a->tile_n != 128)
+    return MOE_ERR_INVALID_ARG;
+  if (need_ws) {
+    if (!a->workspace) return MOE_ERR_INVALID_ARG;
+    if (!aligned(a->workspace, 256)) return MOE_ERR_MISALIGNED;
+    if (a->workspace_bytes < kStatusBytes + expert_ws_layout(a->T, a->H, a->I, a->E, a->k).total)
+      return MOE_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (a->T == 0) return MOE_OK;
+  if (!a->xq || !a->xs || !a->w1q || !a->w1s || !a->w2q || !a->w2s || !a->topk_idx || !a->topk_w || !a->counts ||
+      !a->offsets || !a->perm || !a->y_pairs)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(a->w1q, 32) || !aligned(a->w2q, 32)) return MOE_ERR_MISALIGNED;
+  if (!aligned(a->xq, 16) || !aligned(a->xs, 16) || !aligned(a->w1s, 16) || !aligned(a->w2s, 16) ||
+      !aligned(a->y_pairs, 16) || (a->hq && !aligned(a->hq, 16)))
+    return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+}  // namespace mxq
+
+using namespace mxq;
+
+extern "C" size_t moe_expert_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return 0;
+  return kStatusBytes + expert_ws_layout(T, H, I, E, k).total;
+}
+
+extern "C" int moe_expert_forward(const moe_expert_args *args, cudaStream_t stream) {
+  const int rc = check_expert_args(args, true);
+  if (rc != MOE_OK) return rc;
+  if (cudaMemsetAsync(args->workspace, 0, 8, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_expert_forward(args, reinterpret_cast<int *>(args->workspace),
+                               reinterpret_cast<char *>(args->workspace) + kStatusBytes, stream);
+}

@@ -1,0 +1,84 @@
+// host_common.h -- host-side helpers shared by the C-ABI translation units:
+// argument checks, launch-error mapping, tensor-map encoding through the
+// driver entry point, and the tile-size / workspace arithmetic.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe_mxq.h"
+
+namespace mxq {
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Encodes a 2-D tiled tensor map (dims/strides in elements/bytes as the
+// driver expects).  Returns false if the driver rejects it.
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint64_t dim0, uint64_t dim1,
+                    uint64_t stride1_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz);
+
+// ------------------------------------------------------------------ scratch of
+// the expert GEMMs (offsets are multiples of 256 bytes from the region base).
+struct ExpertWs {
+  size_t sfb1;       // GEMM1 token-scale chunks [max_tiles][H/128][512]
+  size_t sfb2;       // GEMM2 token-scale chunks [max_tiles][I/128][512]
+  size_t hq;         // requantised h in pool order [P][I]
+  size_t total;
+};
+
+inline int64_t max_token_tiles(int64_t P, int64_t E, int64_t bn) {
+  const int64_t ne = E < P ? E : P;
+  return ceil_div(P, bn) + ne;
+}
+
+inline ExpertWs expert_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  const int64_t P = T * k;
+  const int64_t tiles = max_token_tiles(P, E, 16);   // smallest tile -> most tiles
+  ExpertWs w;
+  size_t off = 0;
+  w.sfb1 = off;    off += round_up((size_t)tiles * (size_t)(H / 128) * 512, 256);
+  w.sfb2 = off;    off += round_up((size_t)tiles * (size_t)(I / 128) * 512, 256);
+  w.hq = off;      off += round_up((size_t)P * (size_t)I, 256);
+  w.total = off;
+  return w;
+}
+
+// Every public workspace starts with this many bytes of status words.
+constexpr size_t kStatusBytes = 256;
+
+// Token tile chosen from the mean number of pairs per routed expert.
+inline int choose_tile_n(int64_t P, int64_t E) {
+  const int64_t ne = E < P ? E : P;
+  const int64_t mean = ne > 0 ? ceil_div(P, ne) : 1;
+  if (mean <= 16) return 16;
+  if (mean <= 32) return 32;
+  if (mean <= 64) return 64;
+  return 128;
+}
+
+// Internal launchers (return a moe_status).  `status` points at the two
+// status words of the caller's workspace.
+int launch_quant_act(const uint16_t *x, int64_t rows, int64_t K, uint8_t *q, uint8_t *s, cudaStream_t st);
+int launch_route(const float *logits, int64_t T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
+size_t permute_scratch_bytes(int64_t T, int E, int k);
+int launch_permute(const int32_t *idx, int64_t T, int E, int k, int32_t *counts, int32_t *offsets,
+                   int32_t *perm, int32_t *inv_perm, int *status, void *scratch, cudaStream_t st);
+int check_expert_args(const moe_expert_args *a, bool need_ws);
+int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, cudaStream_t st);
+int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k, int64_t H, uint16_t *y,
+                   cudaStream_t st);
+
+}  // namespace mxq

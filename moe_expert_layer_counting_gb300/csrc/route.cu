@@ -1,0 +1,95 @@
+// route.cu -- softmax top-k routing with renormalisation, one warp per token.
+//
+// MonoMoe kernel -- design, section 1 (phase 1: softmax top-K with optional
+// renormalisation); the MegaMoE test routes with torch.topk over randn
+// scores (Counting Sort / Bucketization in DeepGEMM Mega MoE, section 7.1).
+// Selection ranks raw logits (same set as ranking softmax probabilities);
+// equal logits go to the lower expert index.  Weights are
+// exp(l_j - l_max) / sum over the chosen k -- the full softmax denominator
+// cancels in the renormalisation.
+#include "host_common.h"
+#include "ptx.cuh"
+
+namespace mxq {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kMaxE = 1024;
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restrict__ logits, int64_t T, int E,
+                                                            int k, int32_t *__restrict__ idx,
+                                                            float *__restrict__ w) {
+  extern __shared__ float sm[];                       // kWarps x E logits
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float *row = sm + (size_t)warp * E;
+  for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < T; t += (int64_t)gridDim.x * kWarps) {
+    const float *src = logits + t * E;
+    for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
+    __syncwarp();
+    float my_val = 0.f;   // lane j < k keeps the j-th selection
+    int my_idx = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int e = lane; e < E; e += 32) {
+        const float v = row[e];
+        if (better(v, e, bv, bi)) { bv = v; bi = e; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == j) { my_val = bv; my_idx = bi; }
+      if (lane == (bi & 31)) row[bi] = -INFINITY;     // taken (logits are finite)
+      __syncwarp();
+    }
+    const float lmax = __shfl_sync(0xffffffffu, my_val, 0);
+    const float ex = lane < k ? expf(my_val - lmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+      idx[t * k + lane] = my_idx;
+      w[t * k + lane] = __fdiv_rn(ex, sum);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+int launch_route(const float *logits, int64_t T, int E, int k, int32_t *idx, float *w, cudaStream_t st) {
+  if (T == 0) return MOE_OK;
+  const int64_t blocks = ceil_div(T, kWarps);
+  const int64_t cap = (int64_t)num_sms() * 8;
+  const int grid = (int)(blocks < cap ? blocks : cap);
+  const size_t smem = (size_t)kWarps * E * sizeof(float);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  route_kernel<<<grid, kWarps * 32, smem, st>>>(logits, T, E, k, idx, w);
+  return launch_status();
+}
+
+}  // namespace mxq
+
+using namespace mxq;
+
+extern "C" int moe_route_topk(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *topk_idx,
+                              float *topk_w, cudaStream_t stream) {
+  if (T < 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > kMaxE || k > E || k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned(logits, 16) || !aligned(topk_idx, 16) || !aligned(topk_w, 16)) return MOE_ERR_MISALIGNED;
+  return launch_route(logits, T, E, k, topk_idx, topk_w, stream);
+}
