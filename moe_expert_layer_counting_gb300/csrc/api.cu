@@ -135,7 +135,7 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
       return MOE_ERR_MISALIGNED;
   }
 
-  if (cudaMemsetAsync(ws, 0, 8, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, 32, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (a->T == 0) {
     if (a->counts_out && cudaMemsetAsync(a->counts_out, 0, (size_t)a->E * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (a->offsets_out && cudaMemsetAsync(a->offsets_out, 0, (size_t)(a->E + 1) * 4, st) != cudaSuccess)

@@ -58,7 +58,8 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * BN + 8 * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                          : kTmemCols <= 256 ? 256 : 512;
-  static constexpr uint32_t kTxBytes = kABytes + kBBytes + 512 + kSfbBytes;
+  // the FP4-unpacking TMA load completes the packed (global) byte count: K/2 per row
+  static constexpr uint32_t kTxBytes = kABytes / 2 + kBBytes + 512 + kSfbBytes;
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t *sfa_src = args.w_sf + ((size_t)(ti.e * args.MT + ti.mt) * args.KB) * 512;
       const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB) * 512;
       for (int kb = 0; kb < args.KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb))) {
           ok = false;
           break;
         }
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // never leave with copies in flight: wait for the last load of each stage
     for (int s = 0; s < C::kStages; ++s)
-      if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit);
+      if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit, kWaitProducerDrain, s);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     int stage = 0;
@@ -255,11 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&tmem_empty[acc], acc_phase ^ 1, status, kWaitLimit))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tmem_empty[acc], acc_phase ^ 1, status, kWaitLimit, kWaitMmaTmemEmpty, w))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       for (int kb = 0; kb < args.KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, status, kWaitLimit))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, status, kWaitLimit, kWaitMmaFull, kb))) {
           ok = false;
           break;
         }
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // all MMAs issued by this thread complete before TMEM is released
     if (lane == 0) tc_commit(mma_done);
     __syncwarp();
-    mbar_wait(mma_done, 0, status, kWaitLimit);
+    mbar_wait(mma_done, 0, status, kWaitLimit, kWaitMmaDone, 0);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the four epilogue warps agree on the outcome of the bounded wait before
       // any of them enters another named barrier
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&tmem_full[acc], acc_phase, status, kWaitLimit));
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&tmem_full[acc], acc_phase, status, kWaitLimit, kWaitEpiTmemFull, w));
       if (lane == 0) vote[q] = got ? 1 : 0;
       named_bar_sync(1, kEpiThreads);
       if (!(vote[0] & vote[1] & vote[2] & vote[3])) break;
@@ -548,7 +549,7 @@ extern "C" size_t moe_expert_workspace_size(int64_t T, int64_t H, int64_t I, int
 extern "C" int moe_expert_forward(const moe_expert_args *args, cudaStream_t stream) {
   const int rc = check_expert_args(args, true);
   if (rc != MOE_OK) return rc;
-  if (cudaMemsetAsync(args->workspace, 0, 8, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(args->workspace, 0, 32, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_expert_forward(args, reinterpret_cast<int *>(args->workspace),
                                reinterpret_cast<char *>(args->workspace) + kStatusBytes, stream);
 }

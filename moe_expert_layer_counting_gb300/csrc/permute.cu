@@ -221,7 +221,7 @@ extern "C" int moe_permute(const int32_t *topk_idx, int64_t T, int32_t E, int32_
   if (T > 0 && (!topk_idx || !perm || !inv_perm)) return MOE_ERR_INVALID_ARG;
   if (!aligned(workspace, 256)) return MOE_ERR_MISALIGNED;
   if (workspace_bytes < kStatusBytes + permute_scratch_bytes(T, E, k)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (cudaMemsetAsync(workspace, 0, 8, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 32, stream) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_permute(topk_idx, T, E, k, counts, offsets, perm, inv_perm, reinterpret_cast<int *>(workspace),
                         reinterpret_cast<char *>(workspace) + kStatusBytes, stream);
 }

@@ -8,8 +8,10 @@
 namespace mxq {
 
 // ---------------------------------------------------------------- status words
-// Every workspace starts with two int32 words: [0] first error (0 = ok),
-// [1] abort flag raised by a device-side wait that gave up.
+// Every workspace starts with int32 status words: [0] first error (0 = ok),
+// [1] abort flag raised by a device-side wait that gave up, [2] the site of
+// the first wait that gave up (see the kWait* codes), [3] its block index,
+// [4] its loop position.
 enum : int { kStatusOk = 0, kStatusTimeout = 6, kStatusBadIndex = 7 };
 
 __device__ __forceinline__ void report_status(int *status, int code) {
@@ -55,11 +57,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Sites of bounded waits, recorded in status word [2] on a timeout.
+enum : int {
+  kWaitProducerEmpty = 1,
+  kWaitMmaTmemEmpty = 2,
+  kWaitMmaFull = 3,
+  kWaitEpiTmemFull = 4,
+  kWaitProducerDrain = 5,
+  kWaitMmaDone = 6
+};
+
 // Waits for phase `parity` of `bar` to complete.  Gives up after `limit`
 // clock cycles, or as soon as the abort flag is raised, and returns false.
-// On a timeout it raises the abort flag and records the status itself.
+// On a timeout it raises the abort flag and records the status, the wait
+// site and the loop position `pos` itself.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *ws_status,
-                                          long long limit) {
+                                          long long limit, int site = 0, int pos = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   volatile int *abort_flag = ws_status + 1;
@@ -67,6 +80,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *w
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
+      if (atomicCAS(ws_status + 2, 0, site) == 0) {
+        ws_status[3] = (int)blockIdx.x;
+        ws_status[4] = pos;
+      }
       report_status(ws_status, kStatusTimeout);
       atomicExch(ws_status + 1, 1);
       return false;

@@ -20,8 +20,8 @@ from oracle import formats as F  # noqa: E402
 @functools.lru_cache(maxsize=None)
 def lib():
     """Builds (if stale) and imports the binding."""
-    from moe_expert_layer_counting_gb300 import build as _b
-    _b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     from moe_expert_layer_counting_gb300 import binding
     return binding
 
