@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE expert layer (moe_forward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one moe_forward (activation cast, routing, counting-sort permute,
+GEMM1 + SwiGLU (.) weight + FP8 requantisation, GEMM2, combine) over the
+workload's T tokens, replayed from a CUDA graph.  Default workload: the
+small-expert decode (T=8, H=2048, I=512, E=256, top-8).  Inputs are seeded
+synthetic tensors (workloads/), resident in HBM when timing starts.  L2 is
+flushed between timed steps (512 MiB written, then 512 MiB read, so no dirty
+flush lines are written back inside the timed step).  Each step is bracketed
+by CUDA events on the launching stream; the timed region is bracketed by a
+barrier and torch.cuda.synchronize().
+
+Multi-GPU: the layer does not shard across GPUs here (replicas only): with N
+ranks each GPU runs its own independent replica, value = all ranks' tokens /
+max-over-ranks time, "scaling": "weak".
+
+--impl reference times the CPU oracle (oracle/, float64) on this host's cores
+on a fixed 2-token sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM GB/s)"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="small_decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (for profiler launch lists)")
+    ap.add_argument("--quick", action="store_true", help="skip the CPU-baseline and e2e legs")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampler running while the GPU is busy."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(dev) -> str:
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev.index or 0] if vis else str(dev.index or 0)
+
+
+# ---------------------------------------------------------------- roofline bookkeeping
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic(wl, counts):
+    """Algorithmic bytes / flops of the layer and of each GEMM (one launch)."""
+    touched = int((counts > 0).sum())
+    P = wl.T * wl.k
+    w1 = 2 * wl.I * (wl.H // 2 + wl.H // 32)           # per expert
+    w2 = wl.H * (wl.I // 2 + wl.I // 32)
+    x_q = wl.T * (wl.H + wl.H // 32)                   # FP8 activations + scales
+    h_q = P * (wl.I + wl.I // 32)
+    y_pairs = P * wl.H * 2
+    return {
+        "touched_experts": touched,
+        "layer_bytes": wl.T * wl.H * 2 + wl.T * wl.E * 4 + touched * (w1 + w2) + wl.T * wl.H * 2,
+        "layer_flops": 2 * P * 3 * wl.H * wl.I,
+        "gemm1_bytes": touched * w1 + x_q + h_q,
+        "gemm1_flops": 2 * P * 2 * wl.I * wl.H,
+        "gemm2_bytes": touched * w2 + h_q + y_pairs,
+        "gemm2_flops": 2 * P * wl.H * wl.I,
+    }
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import workloads as W
+    from moe_expert_layer_counting_gb300 import binding as B
+    from moe_expert_layer_counting_gb300.layer import QuantizedExperts
+
+    wl = W.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    x_cpu, logits_cpu = W.tokens(wl)
+    x = x_cpu.to(dev)
+    logits = logits_cpu.to(dev)
+    qe = QuantizedExperts(wl.E, wl.H, wl.I, device=dev)
+    for e in range(wl.E):
+        l1, l2 = W.expert_weights(wl, e, dev)
+        qe.set_expert(e, l1, l2)
+    del l1, l2
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    ws = torch.empty(B.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def forward(st):
+        B.moe_forward(x, logits, qe.w1q, qe.w1s, qe.w2q, qe.w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
+                      counts_out=counts, offsets_out=offsets, perm_out=perm, tile_n=args.tile_n, stream=st)
+
+    def flush():
+        if not args.no_flush:
+            flush_w.zero_()
+            flush_r.sum()
+
+    with torch.cuda.stream(stream):
+        forward(stream)                       # first call outside capture (sets kernel attributes)
+    stream.synchronize()
+    assert B.moe_get_device_status(ws, stream) == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        forward(torch.cuda.current_stream())
+    counts_np = counts.cpu().numpy()
+    # quant, route, permute (count + scatter above 2048 pairs), token scales, GEMM1, GEMM2, combine
+    n_launch_forward = 7 + (1 if T * k > 2048 else 0)
+
+    def timed_loop(step_fn, steps):
+        evs = []
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                flush()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step_fn()
+                b.record(stream)
+                evs.append((a, b))
+        stream.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # warm-up, then a short soak so that the clock sampler sees the GPU under load
+    timed_loop(graph.replay, args.warmup)
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(gpu_id_for(dev)) as clk:
+        t_soak = time.time()
+        while time.time() - t_soak < 1.5:
+            timed_loop(graph.replay, 20)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        times = timed_loop(graph.replay, args.steps)
+        torch.cuda.synchronize()
+        wall = time.time() - t0
+        if world > 1:
+            torch.distributed.barrier()
+    assert B.moe_get_device_status(ws, stream) == 0, "device status word reports an error"
+    total_ms = sum(times)
+    mean_ms = total_ms / len(times)
+    if world > 1:
+        t = torch.tensor([total_ms, mean_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, mean_ms = float(t[0]), float(t[1])
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # per-GEMM timing (dominant kernel) with the layer's own routing
+    ews = torch.empty(B.moe_expert_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
+    xs = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+    y_pairs = torch.empty(k, T, H, dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(stream):
+        B.mxq_quantize_act(x, xq, xs, stream=stream)
+
+    def phase(ph):
+        B.moe_expert_forward(xq, xs, qe.w1q, qe.w1s, qe.w2q, qe.w2s, idx, wts, counts, offsets, perm, y_pairs,
+                             ews, tile_n=args.tile_n, phases=ph, stream=stream)
+
+    with torch.cuda.stream(stream):
+        phase(B.PHASE_TOKEN_SCALES | B.PHASE_GEMM1 | B.PHASE_GEMM2)
+    stream.synchronize()
+    g1 = timed_loop(lambda: phase(B.PHASE_GEMM1), max(args.steps, 20))
+    g2 = timed_loop(lambda: phase(B.PHASE_GEMM2), max(args.steps, 20))
+    assert B.moe_get_device_status(ews, stream) == 0
+    g1_ms, g2_ms = statistics.mean(g1), statistics.mean(g2)
+
+    alg = algorithmic(wl, counts_np)
+    hbm, bf16, peak_src = peaks()
+    fp8_peak_tflops = 2 * bf16                      # FP8 dense = 2x BF16 dense (nominal ratio)
+    dom = "gemm1" if g1_ms >= g2_ms else "gemm2"
+    dom_ms = max(g1_ms, g2_ms)
+    dom_bytes = alg[f"{dom}_bytes"]
+    dom_flops = alg[f"{dom}_flops"]
+    t_bytes = dom_bytes / (hbm * 1e9)
+    t_flops = dom_flops / (fp8_peak_tflops * 1e12)
+    if t_bytes >= t_flops:
+        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4)}
+    else:
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": fp8_peak_tflops, "unit": "TFLOP/s",
+                "frac": round(achieved / fp8_peak_tflops, 4)}
+    roof.update({"kernel": f"expert_gemm_kernel ({dom}, one launch)", "ms": round(dom_ms, 5),
+                 "algorithmic_bytes": dom_bytes, "algorithmic_flops": dom_flops,
+                 "traffic": None, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)"})
+    layer_time_bound = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (fp8_peak_tflops * 1e12))
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic (seeded, workloads/)",
+        "config": {"workload": wl.describe(), "tokens_per_step": T, "pairs": T * k,
+                   "touched_experts": alg["touched_experts"], "tile_n": args.tile_n or "auto",
+                   "l2": "flushed between steps (512 MiB write + 512 MiB read)" if not args.no_flush else "not flushed",
+                   "cuda_graph": True, "parallelism": "replicas" if world > 1 else "single GPU"},
+        "layer_roofline_frac": round(layer_time_bound / (mean_ms * 1e-3), 4),
+        "gemm_ms": {"gemm1": round(g1_ms, 5), "gemm2": round(g2_ms, 5)},
+        "roofline": roof,
+        "gpu_launches": n_launch_forward * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+        "clocks": clk.summary(),
+    }
+
+    if not args.quick:
+        # end to end through the public API with host buffers: H2D inputs, layer, D2H output
+        x_h = x_cpu.pin_memory()
+        l_h = logits_cpu.pin_memory()
+        y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            x.copy_(x_h, non_blocking=True)
+            logits.copy_(l_h, non_blocking=True)
+            graph.replay()
+            y_h.copy_(y, non_blocking=True)
+
+        e2e_times = timed_loop(e2e_step, args.steps)
+        e2e_total = sum(e2e_times)
+        if world > 1:
+            t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_total = float(t[0])
+        result["e2e"] = {"value": round(world * T * args.steps / (e2e_total / 1e3), 1), "unit": UNIT,
+                         "h2d_bytes_per_step": x_h.numel() * 2 + l_h.numel() * 4,
+                         "d2h_bytes_per_step": y_h.numel() * 2}
+        if rank == 0 and world == 1:
+            result["cpu_baseline"] = cpu_baseline(wl, steps=2)
+    return result
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def _oracle_sample(wl, n_tokens=2):
+    """A fixed token sample of the workload and the oracle-quantised experts it needs."""
+    import numpy as np
+    import torch
+
+    import workloads as W
+    from oracle import moe as O
+    x, logits = W.tokens(wl)
+    idx, _ = O.route_topk(logits[:n_tokens].numpy(), wl.k)
+    need = sorted(set(idx.reshape(-1).tolist()))
+    E, H, I = wl.E, wl.H, wl.I
+    w1q = np.zeros((E, 2 * I, H // 2), np.uint8); w1s = np.zeros((E, 2 * I, H // 32), np.uint8)
+    w2q = np.zeros((E, H, I // 2), np.uint8); w2s = np.zeros((E, H, I // 32), np.uint8)
+    for e in need:
+        l1, l2 = W.expert_weights(wl, e, "cpu")
+        q, s = O.quantize_weight(l1.view(torch.int16).numpy().view(np.uint16)[None])
+        w1q[e], w1s[e] = q[0], s[0]
+        q, s = O.quantize_weight(l2.view(torch.int16).numpy().view(np.uint16)[None])
+        w2q[e], w2s[e] = q[0], s[0]
+    xb = x[:n_tokens].view(torch.int16).numpy().view(np.uint16)
+    return xb, logits[:n_tokens].numpy(), (w1q, w1s, w2q, w2s)
+
+
+def _oracle_step(wl, sample):
+    from oracle import moe as O
+    xb, lg, w = sample
+    O.forward(xb, lg, *w, wl.k)
+
+
+def cpu_baseline(wl, steps=2, n_tokens=2):
+    sample = _oracle_sample(wl, n_tokens)
+    _oracle_step(wl, sample)
+    t0 = time.time()
+    for _ in range(steps):
+        _oracle_step(wl, sample)
+    dt = (time.time() - t0) / steps
+    return {"value": round(n_tokens / dt, 3), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{n_tokens} tokens of {wl.describe()} ({n_tokens * wl.k} pairs) per step, float64 "
+                      f"NumPy oracle (weights of the experts they route to quantised untimed), {steps} steps"}
+
+
+def run_reference(args):
+    import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    n_tokens = 2
+    sample = _oracle_sample(wl, n_tokens)
+    for _ in range(args.warmup):
+        _oracle_step(wl, sample)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.time()
+        _oracle_step(wl, sample)
+        times.append(time.time() - t0)
+    total = sum(times)
+    value = n_tokens * args.steps / total
+    cores = len(os.sched_getaffinity(0))
+    sample_txt = (f"{n_tokens} tokens of {wl.describe()} ({n_tokens * wl.k} pairs) per step, float64 NumPy "
+                  f"oracle, weights of the routed experts quantised untimed")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, workloads/)", "config": {"workload": wl.describe(),
+                                                                  "tokens_per_step": n_tokens},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample_txt},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    import __graft_entry__
+    __graft_entry__.build()
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -132,8 +132,22 @@ MOE_API int moe_permute(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k
  *   hq/hs: optional outputs (NULL = not written): the requantised h in pool
  *          order, hq [P][I] e4m3 and hs [P][I/32] ue8m0, row s = pair perm[s].
  *   tile_n: token tile (16, 32, 64, 128) or 0 to let the library choose.
+ *   phases: 0 for the whole layer, or a mask of enum moe_phase to run steps
+ *          separately on the same workspace (same tile_n in every call):
+ *          TOKEN_SCALES gathers GEMM1's token scales into the workspace;
+ *          GEMM1 writes h (to hq if given, else to the workspace) and GEMM2's
+ *          scale chunks; GEMM2 reads them; H_SCALES instead builds GEMM2's
+ *          scale chunks from a caller-provided h (hq and hs required, pool
+ *          order), so that GEMM2 can run on an h computed elsewhere.
  *   workspace: at least moe_expert_workspace_size(...) bytes, 256-byte aligned.
  */
+enum moe_phase {
+    MOE_PHASE_TOKEN_SCALES = 1,
+    MOE_PHASE_GEMM1 = 2,
+    MOE_PHASE_GEMM2 = 4,
+    MOE_PHASE_H_SCALES = 8
+};
+
 typedef struct moe_expert_args {
     uint32_t struct_size;   /* sizeof(moe_expert_args) */
     int64_t T, H, I;
@@ -146,6 +160,7 @@ typedef struct moe_expert_args {
     uint16_t *y_pairs;
     uint8_t *hq, *hs;
     int32_t tile_n;
+    int32_t phases;
     void *workspace;
     size_t workspace_bytes;
 } moe_expert_args;

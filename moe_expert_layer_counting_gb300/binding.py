@@ -35,6 +35,7 @@ MOE_ERR_TIMEOUT = 6
 MOE_ERR_DEVICE_INDEX = 7
 
 LAYOUT_CANONICAL, LAYOUT_MMA_L1, LAYOUT_MMA_L2 = 0, 1, 2
+PHASE_TOKEN_SCALES, PHASE_GEMM1, PHASE_GEMM2, PHASE_H_SCALES = 1, 2, 4, 8
 
 EXPORTED = ["mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_permute_workspace_size",
             "moe_permute", "moe_expert_workspace_size", "moe_expert_forward", "moe_combine",
@@ -50,7 +51,7 @@ class MoeExpertArgs(ctypes.Structure):
                 ("topk_idx", _p), ("topk_w", _p),
                 ("counts", _p), ("offsets", _p), ("perm", _p),
                 ("y_pairs", _p), ("hq", _p), ("hs", _p),
-                ("tile_n", _i32),
+                ("tile_n", _i32), ("phases", _i32),
                 ("workspace", _p), ("workspace_bytes", _sz)]
 
 
@@ -165,7 +166,8 @@ def moe_expert_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
 
 
 def moe_expert_forward(xq, xs, w1q, w1s, w2q, w2s, topk_idx, topk_w, counts, offsets, perm, y_pairs,
-                       workspace, hq=None, hs=None, tile_n: int = 0, stream=None, check=True) -> int:
+                       workspace, hq=None, hs=None, tile_n: int = 0, phases: int = 0, stream=None,
+                       check=True) -> int:
     T, H = xq.shape
     E = w1q.shape[0]
     I = w2q.shape[2] * 2
@@ -173,7 +175,7 @@ def moe_expert_forward(xq, xs, w1q, w1s, w2q, w2s, topk_idx, topk_w, counts, off
     a = MoeExpertArgs(ctypes.sizeof(MoeExpertArgs), T, H, I, E, k,
                       _ptr(xq), _ptr(xs), _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s),
                       _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(perm),
-                      _ptr(y_pairs), _ptr(hq), _ptr(hs), tile_n,
+                      _ptr(y_pairs), _ptr(hq), _ptr(hs), tile_n, phases,
                       _ptr(workspace), workspace.numel() * workspace.element_size())
     rc = lib.moe_expert_forward(ctypes.byref(a), _stream(stream))
     if check:

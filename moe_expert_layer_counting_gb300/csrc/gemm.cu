@@ -404,15 +404,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Token-scale chunks of GEMM1: for pool row s (tile g, row r) copy the 4
-// scale bytes of K block kb of token perm[s]/k into chunk (g, kb) at byte
-// (r%32)*16 + (r/32)*4.
-template <int BN>
-__global__ void __launch_bounds__(256) prep_sfb1_kernel(const uint8_t *__restrict__ xs,
-                                                        const int32_t *__restrict__ counts,
-                                                        const int32_t *__restrict__ offsets,
-                                                        const int32_t *__restrict__ perm, int E, int k, int KB,
-                                                        uint8_t *__restrict__ sfb1) {
+// Scale chunks of a GEMM's token operand.  For pool row s (tile g, row r)
+// copy the 4 scale bytes of K block kb into chunk (g, kb) at byte
+// (r%32)*16 + (r/32)*4.  GEMM1 takes them from the activation scales of token
+// perm[s]/k (FROM_TOKENS); GEMM2 fed with an external h takes them from row s
+// of that h's scales.
+template <int BN, bool FROM_TOKENS>
+__global__ void __launch_bounds__(256) prep_scale_chunks_kernel(const uint8_t *__restrict__ src_scales,
+                                                                const int32_t *__restrict__ counts,
+                                                                const int32_t *__restrict__ offsets,
+                                                                const int32_t *__restrict__ perm, int E, int k,
+                                                                int KB, uint8_t *__restrict__ chunks) {
   extern __shared__ int sh[];
   int *tile_off = sh, *cnt_sm = sh + (E + 1), *off_sm = sh + 2 * (E + 1);
   if (threadIdx.x < 32) build_tile_map<BN>(counts, offsets, E, tile_off, cnt_sm, off_sm);
@@ -421,22 +423,32 @@ __global__ void __launch_bounds__(256) prep_sfb1_kernel(const uint8_t *__restric
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   for (int s = blockIdx.x * nwarps + warp; s < P; s += gridDim.x * nwarps) {
-    int lo = 0, hi = E;
+    int lo = 0, hi = E;                        // expert e with off[e] <= s < off[e+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (off_sm[mid] <= s) lo = mid; else hi = mid;
     }
-    // skip empty experts that share the same offset
-    while (lo + 1 < E && off_sm[lo + 1] <= s) ++lo;
     const int rank = s - off_sm[lo];
     const int g = tile_off[lo] + rank / BN, r = rank % BN;
-    const int t = __ldg(perm + s) / k;
-    const uint32_t *src = reinterpret_cast<const uint32_t *>(xs + (size_t)t * KB * 4);
+    const int row = FROM_TOKENS ? __ldg(perm + s) / k : s;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(src_scales + (size_t)row * KB * 4);
     for (int kb = lane; kb < KB; kb += 32) {
       const uint32_t wv = __ldg(src + kb);
-      *reinterpret_cast<uint32_t *>(sfb1 + ((size_t)g * KB + kb) * 512 + (r & 31) * 16 + (r >> 5) * 4) = wv;
+      *reinterpret_cast<uint32_t *>(chunks + ((size_t)g * KB + kb) * 512 + (r & 31) * 16 + (r >> 5) * 4) = wv;
     }
   }
+}
+
+template <int BN, bool FROM_TOKENS>
+int launch_prep(const uint8_t *src, const moe_expert_args *a, int KB, uint8_t *chunks, cudaStream_t st) {
+  const int64_t P = a->T * a->k;
+  const size_t sm = (size_t)3 * (a->E + 1) * 4;
+  const int64_t blocks = ceil_div(P, 8);
+  const int cap = num_sms() * 4;
+  const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+  prep_scale_chunks_kernel<BN, FROM_TOKENS><<<grid, 256, sm, st>>>(src, a->counts, a->offsets, a->perm, a->E, a->k,
+                                                                   KB, chunks);
+  return launch_status();
 }
 
 template <int BN>
@@ -446,52 +458,57 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   uint8_t *hq = a->hq ? a->hq : reinterpret_cast<uint8_t *>(ws + lay.hq);
   const int64_t P = a->T * a->k;
   const int E = a->E;
+  const int phases = a->phases ? a->phases : (MOE_PHASE_TOKEN_SCALES | MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2);
 
-  // 1. token-scale chunks for GEMM1
-  {
-    const size_t sm = (size_t)3 * (E + 1) * 4;
-    const int64_t blocks = ceil_div(P, 8);
-    const int grid = (int)(blocks < num_sms() * 4 ? (blocks > 0 ? blocks : 1) : num_sms() * 4);
-    prep_sfb1_kernel<BN><<<grid, 256, sm, st>>>(a->xs, a->counts, a->offsets, a->perm, E, a->k, (int)(a->H / 128),
-                                                 sfb1);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-  }
-
-  // 2. tensor maps
-  CUtensorMap tw1, tx, tw2, th;
-  bool ok = encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, (uint64_t)a->H,
-                           (uint64_t)E * 2 * a->I, (uint64_t)a->H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a->xq, (uint64_t)a->H, (uint64_t)a->T,
-                            (uint64_t)a->H, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, (uint64_t)a->I,
-                            (uint64_t)E * a->H, (uint64_t)a->I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
-                            (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return MOE_ERR_CUDA;
+  // token-scale chunks of GEMM1 (gathered by pair id)
+  if ((phases & MOE_PHASE_TOKEN_SCALES) &&
+      launch_prep<BN, true>(a->xs, a, (int)(a->H / 128), sfb1, st) != MOE_OK)
+    return MOE_ERR_CUDA;
+  // scale chunks of GEMM2 from a caller-provided h (instead of GEMM1's epilogue)
+  if ((phases & MOE_PHASE_H_SCALES) && launch_prep<BN, false>(a->hs, a, (int)(a->I / 128), sfb2, st) != MOE_OK)
+    return MOE_ERR_CUDA;
 
   GemmArgs g{};
   g.E = E; g.k = a->k; g.T = (int)a->T; g.H = (int)a->H; g.I = (int)a->I;
   g.counts = a->counts; g.offsets = a->offsets; g.perm = a->perm; g.topk_w = a->topk_w;
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
-
   const size_t sm = smem_bytes<BN>(E);
   const int grid = num_sms();
-  // 3. GEMM1 + SwiGLU (.) weight + FP8 requantisation
-  g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
-  g.w_sf = a->w1s; g.b_sf = sfb1;
-  if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  expert_gemm_kernel<BN, 1><<<grid, kThreads, sm, st>>>(tw1, tx, g);
-  if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-  // 4. GEMM2 -> BF16 per pair
-  g.M = (int)a->H; g.K = (int)a->I; g.KB = (int)(a->I / 128); g.MT = (int)(a->H / 128);
-  g.w_sf = a->w2s; g.b_sf = sfb2;
-  if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  expert_gemm_kernel<BN, 2><<<grid, kThreads, sm, st>>>(tw2, th, g);
-  return launch_status();
+
+  if (phases & MOE_PHASE_GEMM1) {
+    // GEMM1 + SwiGLU (.) weight + FP8 requantisation
+    CUtensorMap tw1, tx;
+    bool ok = encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, (uint64_t)a->H,
+                             (uint64_t)E * 2 * a->I, (uint64_t)a->H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a->xq, (uint64_t)a->H, (uint64_t)a->T,
+                              (uint64_t)a->H, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return MOE_ERR_CUDA;
+    g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
+    g.w_sf = a->w1s; g.b_sf = sfb1;
+    if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    expert_gemm_kernel<BN, 1><<<grid, kThreads, sm, st>>>(tw1, tx, g);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  if (phases & MOE_PHASE_GEMM2) {
+    // GEMM2 -> BF16 per pair
+    CUtensorMap tw2, th;
+    bool ok = encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, (uint64_t)a->I,
+                             (uint64_t)E * a->H, (uint64_t)a->I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
+                              (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return MOE_ERR_CUDA;
+    g.M = (int)a->H; g.K = (int)a->I; g.KB = (int)(a->I / 128); g.MT = (int)(a->H / 128);
+    g.w_sf = a->w2s; g.b_sf = sfb2;
+    g.hs_out = nullptr;
+    if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    expert_gemm_kernel<BN, 2><<<grid, kThreads, sm, st>>>(tw2, th, g);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 }  // namespace
@@ -520,6 +537,8 @@ int check_expert_args(const moe_expert_args *a, bool need_ws) {
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a->tile_n != 0 && a->tile_n != 16 && a->tile_n != 32 && a->tile_n != 64 && a->tile_n != 128)
     return MOE_ERR_INVALID_ARG;
+  if (a->phases & ~15) return MOE_ERR_INVALID_ARG;
+  if ((a->phases & MOE_PHASE_H_SCALES) && (!a->hq || !a->hs)) return MOE_ERR_INVALID_ARG;
   if (need_ws) {
     if (!a->workspace) return MOE_ERR_INVALID_ARG;
     if (!aligned(a->workspace, 256)) return MOE_ERR_MISALIGNED;

@@ -200,3 +200,31 @@ def test_large_workloads_sampled(B, wl_name):
         acc = acc + np.where((st.idx_ref[:, j] >= 0)[:, None], yp[j], np.float32(0))
     want = torch.from_numpy(acc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(y_fwd, want)
+
+
+@pytest.mark.parametrize("wl_name,tile_n", [("tiny", 16), ("tiny", 128), ("small_decode", 0)])
+def test_gemm2_on_oracle_h(B, wl_name, tile_n):
+    """GEMM2 alone, fed with the oracle's own requantised h (pool order): the
+    only difference left is FP32 accumulation before the BF16 cast, so the
+    per-pair rows agree to one BF16 ulp, and almost all bit for bit."""
+    st = Setup(B, W.WORKLOADS[wl_name])
+    wl = st.wl
+    y_ref, hq_ref, hs_ref = st.oracle_pairs()
+    dev = "cuda"
+    perm = st.perm_ref
+    hq = torch.from_numpy(np.ascontiguousarray(hq_ref[perm])).to(dev)
+    hs = torch.from_numpy(np.ascontiguousarray(hs_ref[perm])).to(dev)
+    y_pairs = torch.zeros(wl.k, wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(B.moe_expert_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.k), dtype=torch.uint8, device=dev)
+    t = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
+    B.moe_expert_forward(t(st.xq_ref), t(st.xs_ref), st.qe.w1q, st.qe.w1s, st.qe.w2q, st.qe.w2s, t(st.idx_ref),
+                         t(st.w_ref), t(st.counts_ref), t(st.offsets_ref), t(perm), y_pairs, ws, hq=hq, hs=hs,
+                         tile_n=tile_n, phases=B.PHASE_H_SCALES | B.PHASE_GEMM2)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ws) == 0
+    pairs = np.nonzero(st.idx_ref.reshape(-1) >= 0)[0]
+    tt, jj = pairs // wl.k, pairs % wl.k
+    g = F.bf16_bits_to_f64(Hp.bits16(y_pairs)[jj, tt])
+    r = F.bf16_bits_to_f64(y_ref[jj, tt])
+    assert np.all(np.abs(g - r) <= np.abs(r) * 2.0 ** -7 + 1e-30)
+    assert np.mean(g != r) <= 1e-2
