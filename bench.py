@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (for profiler launch lists)")
     ap.add_argument("--quick", action="store_true", help="skip the CPU-baseline and e2e legs")
+    ap.add_argument("--launch-list", action="store_true",
+                    help="profiler mode: only warm-up + timed graph replays, no flush, soak or extra legs")
     return ap.parse_args()
 
 
@@ -218,6 +220,11 @@ def run_ours(args, rank, world, local_rank):
                 evs.append((a, b))
         stream.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
+
+    if args.launch_list:
+        timed_loop(graph.replay, args.warmup + args.steps)
+        torch.cuda.synchronize()
+        return {"launch_list": True, "workload": wl.describe(), "replays": args.warmup + args.steps}
 
     # warm-up, then a short soak so that the clock sampler sees the GPU under load
     timed_loop(graph.replay, args.warmup)
@@ -402,6 +409,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.launch_list:
+        args.no_flush = True
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
