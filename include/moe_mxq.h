@@ -118,6 +118,30 @@ MOE_API int moe_permute(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k
                 int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* moe_permute for callers that cannot allocate device memory (no counterpart
+ * on the pages).  Some callers have no workspace to give: plugins inside a
+ * host framework that owns every device allocation, or serving loops that
+ * must not call cudaMalloc while they run.  Same inputs, outputs and results
+ * as moe_permute, but the scratch (status words and the per-block expert
+ * histogram) is a file-scope device array of the library: 256 bytes plus
+ * MOE_PERMUTE_NOALLOC_MAX_HIST_BYTES, held by every GPU that loads the
+ * library until the process exits.  Nothing is allocated or freed.
+ *   device_status: optional caller-owned device int32 (NULL = not reported);
+ *     set to 0 by the call, then to MOE_ERR_DEVICE_INDEX if an index >= E
+ *     was seen.
+ * Errors: MOE_ERR_UNSUPPORTED_SHAPE when the histogram would exceed the
+ * array (moe_permute_workspace_size(T,E,k) - 256 > the maximum, e.g. E = 1024
+ * with more than 32768 pairs); MOE_ERR_CUDA if the array's device address
+ * cannot be looked up.
+ * The first call on each device looks up the array's address (once, with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the array, which keeps the last call's
+ * contents: calls that overlap on the GPU race. */
+#define MOE_PERMUTE_NOALLOC_MAX_HIST_BYTES 65536
+MOE_API int moe_permute_noalloc(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k,
+                                int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                                int32_t *device_status, cudaStream_t stream);
+
 /* Grouped expert GEMMs: GEMM1 (FP8 x FP4 W1|W3, FP32 accumulate) with the
  * fused epilogue h = silu(gate) * up * topk_w, requantised to E4M3 + UE8M0
  * per 32 along I; then GEMM2 (FP8 h x FP4 W2) cast to BF16 per pair.

@@ -38,7 +38,7 @@ LAYOUT_CANONICAL, LAYOUT_MMA_L1, LAYOUT_MMA_L2 = 0, 1, 2
 PHASE_TOKEN_SCALES, PHASE_GEMM1, PHASE_GEMM2, PHASE_H_SCALES = 1, 2, 4, 8
 
 EXPORTED = ["mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_permute_workspace_size",
-            "moe_permute", "moe_expert_workspace_size", "moe_expert_forward", "moe_combine",
+            "moe_permute", "moe_permute_noalloc", "moe_expert_workspace_size", "moe_expert_forward", "moe_combine",
             "moe_workspace_size", "moe_forward", "moe_get_device_status", "moe_status_string", "moe_version"]
 
 
@@ -74,6 +74,7 @@ lib.moe_route_topk.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p]
 lib.moe_permute_workspace_size.argtypes = [_i64, _i32, _i32]
 lib.moe_permute_workspace_size.restype = _sz
 lib.moe_permute.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p, _p, _p, _sz, _p]
+lib.moe_permute_noalloc.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p, _p, _p, _p]
 lib.moe_expert_workspace_size.argtypes = [_i64, _i64, _i64, _i32, _i32]
 lib.moe_expert_workspace_size.restype = _sz
 lib.moe_expert_forward.argtypes = [ctypes.POINTER(MoeExpertArgs), _p]
@@ -85,7 +86,8 @@ lib.moe_get_device_status.argtypes = [_p, _p, ctypes.POINTER(ctypes.c_int)]
 lib.moe_status_string.argtypes = [ctypes.c_int]
 lib.moe_status_string.restype = ctypes.c_char_p
 lib.moe_version.restype = ctypes.c_char_p
-for _name in ("mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_permute", "moe_expert_forward",
+for _name in ("mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_permute", "moe_permute_noalloc",
+              "moe_expert_forward",
               "moe_combine", "moe_forward", "moe_get_device_status"):
     getattr(lib, _name).restype = ctypes.c_int
 
@@ -158,6 +160,18 @@ def moe_permute(topk_idx: torch.Tensor, E: int, counts, offsets, perm, inv_perm,
                          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if check:
         _check(rc, "moe_permute")
+    return rc
+
+
+def moe_permute_noalloc(topk_idx: torch.Tensor, E: int, counts, offsets, perm, inv_perm, device_status=None,
+                        stream=None, check=True) -> int:
+    """moe_permute without a workspace: the scratch is the library's own
+    device array (see include/moe_mxq.h for the size limit and sharing rules)."""
+    T, k = topk_idx.shape
+    rc = lib.moe_permute_noalloc(_ptr(topk_idx), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm),
+                                 _ptr(inv_perm), _ptr(device_status), _stream(stream))
+    if check:
+        _check(rc, "moe_permute_noalloc")
     return rc
 
 
