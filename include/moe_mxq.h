@@ -70,12 +70,15 @@ enum moe_status {
  *   [I,2I) in the input): rows are interleaved in groups of 8, gate then up
  *   (MegaMoE (study notes), "_interleave_l1_weights (gran = 8)"): stored row
  *   r = 16b + c holds input row 8b + c when c < 8 and row I + 8b + c - 8
- *   otherwise.  Codes are [G][N][K/2] in stored-row order.  Scales are in
- *   MMA chunk order: [G][N/128][K/128][512], where byte
+ *   otherwise.  Codes are stored in tile-contiguous blocks
+ *   [G][N/128][K/128][128][64]: block (g, nt, kb) holds stored rows
+ *   128*nt .. 128*nt+127, K values 128*kb .. 128*kb+127, each row packed in
+ *   64 bytes, so one 128 x 128 weight tile is 8 KB in one piece.  Scales are
+ *   in MMA chunk order: [G][N/128][K/128][512], where byte
  *   (r%32)*16 + (r/32)*4 + kk of chunk (g, nt, kb) is the scale of stored row
  *   128*nt + r, K-group 4*kb + kk.  N must be a multiple of 128.
- * MXQ_LAYOUT_MMA_L2 (GEMM2 weights): rows in input order, scales in the same
- *   chunk order.
+ * MXQ_LAYOUT_MMA_L2 (GEMM2 weights): rows in input order, codes and scales
+ *   in the same tile-contiguous / chunk orders.
  */
 enum mxq_layout { MXQ_LAYOUT_CANONICAL = 0, MXQ_LAYOUT_MMA_L1 = 1, MXQ_LAYOUT_MMA_L2 = 2 };
 

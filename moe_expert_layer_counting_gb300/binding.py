@@ -14,7 +14,10 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_mxq.so")
+# MOE_MXQ_LIB may point at another build of the same library (e.g. one built
+# with -DMOE_MXQ_WAIT_STATS for wait-time accounting).
+_LIB_PATH = os.environ.get("MOE_MXQ_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                          "libmoe_mxq.so")
 
 if not os.path.exists(_LIB_PATH):
     raise ImportError(

@@ -33,6 +33,8 @@
 // tiles of one expert) or a token tile (weight tiles of one expert) in L2.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "host_common.h"
 #include "ptx.cuh"
 
@@ -47,25 +49,36 @@ constexpr int kEpiThreads = 128;
 constexpr int kChunk = 16;                    // accumulator columns per epilogue step
 constexpr long long kWaitLimit = 2000000000LL;
 constexpr int kMaxE = 1024;
+constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in HBM (8 KB)
+
+// A pipeline stage covers kKBS K blocks of 128 (256 K): one TMA box of 256
+// weight rows (two consecutive tiles of the tile-contiguous layout), one bulk
+// copy per scale operand and one 2-D box of token rows per K block.  Every
+// asynchronous instruction costs tens of issue cycles in the producer and MMA
+// warps, so fewer, larger copies per byte of weights is what keeps
+// decode-sized tiles streaming.
+constexpr int kKBS = 2;
 
 template <int BN>
 struct Cfg {
-  static constexpr int kABytes = kBM * kBK;                 // unpacked FP4 (8-bit containers)
-  static constexpr int kBBytes = BN * kBK;
-  static constexpr int kSfbBytes = (BN < 32 ? BN : 32) * 16;
-  static constexpr int kStageBytes = kABytes + kBBytes + 1024;
-  static constexpr int kStages = (200 * 1024 / kStageBytes) > 12 ? 12 : (200 * 1024 / kStageBytes);
-  static constexpr int kTmemCols = 2 * BN + 8 * kStages;
+  static constexpr int kATile = kBM * kBK;                  // one unpacked FP4 tile (8-bit containers)
+  static constexpr int kBTile = BN * kBK;
+  static constexpr int kABytes = kKBS * kATile;
+  static constexpr int kBBytes = kKBS * kBTile;
+  static constexpr int kSfbBytes = (BN < 32 ? BN : 32) * 16; // used bytes of a token-scale chunk
+  static constexpr int kStageBytes = kABytes + kBBytes + kKBS * 1024;
+  static constexpr int kStages = (200 * 1024 / kStageBytes) > 8 ? 8 : (200 * 1024 / kStageBytes);
+  static constexpr int kTmemCols = 2 * BN + 8 * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                          : kTmemCols <= 256 ? 256 : 512;
-  // the FP4-unpacking TMA load completes the packed (global) byte count: K/2 per row
-  static constexpr uint32_t kTxBytes = kABytes / 2 + kBBytes + 512 + kSfbBytes;
+  // decode-sized tiles: optional L2 prefetch distance (stages) of weight tiles
+  static constexpr int kDefaultPrefetchStages = 0;
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
-  static constexpr int kOffSfb = kOffSfa + kStages * 512;
-  static constexpr int kOffEpi = kOffSfb + kStages * 512;   // 4 KB epilogue staging
+  static constexpr int kOffSfb = kOffSfa + kStages * kKBS * 512;
+  static constexpr int kOffEpi = kOffSfb + kStages * kKBS * 512;   // 4 KB epilogue staging
   static constexpr int kOffRow = kOffEpi + 4096;            // pair id [BN] + weight [BN]
   static constexpr int kOffBar = kOffRow + 8 * BN;
   static constexpr int kNumBars = 2 * kStages + 5;
@@ -82,8 +95,11 @@ size_t smem_bytes(int E) {
 struct GemmArgs {
   int E, k, T, H, I;
   int M, K, KB, MT;                 // weight rows / reduction / K blocks / weight tiles per expert
+  int prefetch_stages;              // L2 prefetch distance of weight tiles, in stages (0 = off)
   const int32_t *counts, *offsets, *perm;
-  const float *topk_w;
+  const int32_t *tok_pool;          // token of each pool row (GEMM1 gather)
+  const float *w_pool;              // top-k weight of each pool row (GEMM1 epilogue)
+  const uint8_t *w_codes;           // weight codes, tile-contiguous (L2 prefetch)
   const uint8_t *w_sf;              // [E][MT][KB][512]
   const uint8_t *b_sf;              // [tiles][KB][512]
   uint8_t *hq;                      // L1 out [P][I] (pool order)
@@ -97,34 +113,34 @@ struct TileInfo {
   int e, mt, g, s0, valid;
 };
 
-// Exclusive prefix of ceil(counts[e] / BN) computed by one warp into
-// tile_off[0..E]; also copies counts and offsets to shared memory.
+// counts/offsets -> shared memory with independent loads by every thread of
+// the block (no chain of dependent global loads in the prologue).
+__device__ __forceinline__ void load_expert_table(const int32_t *counts, const int32_t *offsets, int E,
+                                                  int *cnt_sm, int *off_sm) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    if (e < E) cnt_sm[e] = __ldg(counts + e);
+    off_sm[e] = __ldg(offsets + e);
+  }
+}
+
+// Exclusive prefix of ceil(cnt_sm[e] / BN) by one warp, from shared memory.
 template <int BN>
-__device__ void build_tile_map(const int32_t *counts, const int32_t *offsets, int E, int *tile_off, int *cnt_sm,
-                               int *off_sm) {
+__device__ void scan_tile_map(const int *cnt_sm, int E, int *tile_off) {
   const int lane = threadIdx.x & 31;
   int carry = 0;
   for (int b = 0; b < E; b += 32) {
     const int e = b + lane;
-    const int c = e < E ? __ldg(counts + e) : 0;
-    const int nt = (c + BN - 1) / BN;
+    const int nt = e < E ? (cnt_sm[e] + BN - 1) / BN : 0;
     int inc = nt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += n;
     }
-    if (e < E) {
-      tile_off[e] = carry + inc - nt;
-      cnt_sm[e] = c;
-      off_sm[e] = __ldg(offsets + e);
-    }
+    if (e < E) tile_off[e] = carry + inc - nt;
     carry += __shfl_sync(0xffffffffu, inc, 31);
   }
-  if (lane == 0) {
-    tile_off[E] = carry;
-    off_sm[E] = __ldg(offsets + E);
-  }
+  if (lane == 0) tile_off[E] = carry;
 }
 
 template <int BN>
@@ -149,6 +165,24 @@ __device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int 
   return ti;
 }
 
+// Optional wait-time accounting (build with -DMOE_MXQ_WAIT_STATS): each role
+// adds the clock cycles it spent in bounded waits, and its total, to 64-bit
+// counters at byte 64 of the status area: [0] producer on empty stages,
+// [1] MMA on full stages, [2] MMA on free accumulators, [3] epilogue on full
+// accumulators, [4] kernel cycles of warp 0, [5] kernel cycles of warp 1,
+// [6] kernel cycles of warp 2, [7] work items.
+#ifdef MOE_MXQ_WAIT_STATS
+#define MXQ_TIMED_WAIT(slot, expr)                                   \
+  ([&]() {                                                           \
+    const long long _t0 = clock64();                                 \
+    const bool _r = (expr);                                          \
+    if (lane == 0) wait_acc[slot] += clock64() - _t0;                \
+    return _r;                                                       \
+  }())
+#else
+#define MXQ_TIMED_WAIT(slot, expr) (expr)
+#endif
+
 template <int BN, int PHASE>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
@@ -164,18 +198,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *tmem_empty = tmem_full + 2;
   uint64_t *mma_done = tmem_full + 4;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::kOffTmemPtr);
+  int *vote = reinterpret_cast<int *>(smem + C::kOffTmemPtr + 4);     // [4], one per epilogue warp
   int *tile_off = reinterpret_cast<int *>(smem + C::kOffExp);
   int *cnt_sm = tile_off + (args.E + 1);
   int *off_sm = cnt_sm + (args.E + 1);
   int32_t *row_pair = reinterpret_cast<int32_t *>(smem + C::kOffRow);
   float *row_w = reinterpret_cast<float *>(smem + C::kOffRow + 4 * BN);
-  int *vote = reinterpret_cast<int *>(smem + C::kOffTmemPtr + 4);     // [4], one per epilogue warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int *status = args.status;
+#ifdef MOE_MXQ_WAIT_STATS
+  long long wait_acc[4] = {0, 0, 0, 0};
+  const long long k_t0 = clock64();
+  int n_items = 0;
+#endif
 
+  load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm);
   if (warp == 0) {
-    build_tile_map<BN>(args.counts, args.offsets, args.E, tile_off, cnt_sm, off_sm);
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
       tma_prefetch_desc(&tmap_b);
@@ -197,6 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_ptr, C::kTmemAlloc);
     tmem_relinquish();
   }
+  __syncthreads();
+  if (warp == 0) scan_tile_map<BN>(cnt_sm, args.E, tile_off);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -209,37 +250,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;
     bool ok = true;
+    // L2 prefetch cursor over this CTA's (work item, K block) sequence; it runs
+    // kPrefetchStages stages ahead of the loads (decode-sized tiles only).
+    int pf_w = blockIdx.x, pf_kb = 0;
+    TileInfo pf_ti{};
+    const int pf_dist = args.prefetch_stages;
+    if (pf_dist > 0 && pf_w < total_work)
+      pf_ti = decode_work<BN>(pf_w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+    auto pf_step = [&](bool issue) {
+      if (pf_w >= total_work) return;
+      const int nk = min(kKBS, args.KB - pf_kb);
+      if (issue && lane == 0) {
+        const size_t t = ((size_t)(pf_ti.e * args.MT + pf_ti.mt) * args.KB + pf_kb);
+        prefetch_l2_bulk(args.w_codes + t * kWTileBytes, nk * kWTileBytes);
+        prefetch_l2_bulk(args.w_sf + t * 512, nk * 512);
+      }
+      pf_kb += nk;
+      if (pf_kb == args.KB) {
+        pf_kb = 0;
+        pf_w += gridDim.x;
+        if (pf_w < total_work) pf_ti = decode_work<BN>(pf_w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      }
+    };
+    if (pf_dist > 0) {
+      for (int i = 0; i < C::kStages; ++i) pf_step(false);        // those go straight to shared memory
+      for (int i = 0; i < pf_dist; ++i) pf_step(true);
+    }
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
       const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
-      int tok[4] = {0, 0, 0, 0};
-      if (PHASE == 1 && lane < BN / 4) {
-        const int first = __ldg(args.perm + ti.s0) / args.k;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = lane * 4 + i;
-          tok[i] = r < ti.valid ? __ldg(args.perm + ti.s0 + r) / args.k : first;
-        }
-      }
-      const int wrow = ti.e * args.M + ti.mt * kBM;
-      const uint8_t *sfa_src = args.w_sf + ((size_t)(ti.e * args.MT + ti.mt) * args.KB) * 512;
+      const int wtile = (ti.e * args.MT + ti.mt) * args.KB;        // first weight tile of this item
+      const uint8_t *sfa_src = args.w_sf + (size_t)wtile * 512;
       const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB) * 512;
-      for (int kb = 0; kb < args.KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb))) {
+      for (int kb = 0; kb < args.KB; kb += kKBS) {
+        const int nk = min(kKBS, args.KB - kb);                   // K blocks in this stage
+        if (!__all_sync(0xffffffffu,
+                        MXQ_TIMED_WAIT(0, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb)))) {
           ok = false;
           break;
         }
         unsigned char *a_dst = smem + C::kOffA + stage * C::kABytes;
         unsigned char *b_dst = smem + C::kOffB + stage * C::kBBytes;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], C::kTxBytes);
-          tma_load_2d(a_dst, &tmap_w, &full[stage], kb * kBK, wrow);
-          bulk_load(smem + C::kOffSfa + stage * 512, sfa_src + (size_t)kb * 512, 512, &full[stage]);
-          bulk_load(smem + C::kOffSfb + stage * 512, sfb_src + (size_t)kb * 512, C::kSfbBytes, &full[stage]);
-          if (PHASE == 2) tma_load_2d(b_dst, &tmap_b, &full[stage], kb * kBK, ti.s0);
+          // the weight box always spans kKBS tiles (rows past the tensor read as zeros);
+          // the FP4-unpacking load completes the packed byte count
+          const uint32_t sfb_bytes = (uint32_t)((nk - 1) * 512 + C::kSfbBytes);
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(kKBS * kWTileBytes + nk * C::kBTile + nk * 512) + sfb_bytes);
+          tma_load_2d(a_dst, &tmap_w, &full[stage], 0, (wtile + kb) * kBM);
+          bulk_load(smem + C::kOffSfa + stage * kKBS * 512, sfa_src + (size_t)kb * 512, nk * 512, &full[stage]);
+          bulk_load(smem + C::kOffSfb + stage * kKBS * 512, sfb_src + (size_t)kb * 512, sfb_bytes, &full[stage]);
+          for (int i = 0; i < nk; ++i)
+            tma_load_2d(b_dst + i * C::kBTile, &tmap_b, &full[stage], (kb + i) * kBK, ti.s0);
         }
         __syncwarp();
-        if (PHASE == 1 && lane < BN / 4)
-          tma_gather4(b_dst + lane * 4 * kBK, &tmap_b, &full[stage], kb * kBK, tok[0], tok[1], tok[2], tok[3]);
+        if (pf_dist > 0) pf_step(true);
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -247,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // never leave with copies in flight: wait for the last load of each stage
     for (int s = 0; s < C::kStages; ++s)
-      if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit, kWaitProducerDrain, s);
+      if (issued_mask & (1u << s))
+        mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit, kWaitProducerDrain, s);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     int stage = 0;
@@ -256,29 +320,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&tmem_empty[acc], acc_phase ^ 1, status, kWaitLimit, kWaitMmaTmemEmpty, w))) break;
+      const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      // MMA N covers the valid tokens of the tile, rounded up to 16
+      const uint32_t n_mma = (uint32_t)min(BN, (ti.valid + 15) & ~15);
+      if (!__all_sync(0xffffffffu,
+                      MXQ_TIMED_WAIT(2, mbar_wait(&tmem_empty[acc], acc_phase ^ 1, status, kWaitLimit, kWaitMmaTmemEmpty, w))))
+        break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < args.KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, status, kWaitLimit, kWaitMmaFull, kb))) {
+      for (int kb = 0; kb < args.KB; kb += kKBS) {
+        const int nk = min(kKBS, args.KB - kb);
+        if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(1, mbar_wait(&full[stage], phase, status, kWaitLimit, kWaitMmaFull, kb)))) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + 8 * stage);
-          const uint32_t sfa = smem_u32(smem + C::kOffSfa + stage * 512);
-          const uint32_t sfb = smem_u32(smem + C::kOffSfb + stage * 512);
-          tc_cp_32x128b_warpx4(sf_col, make_smem_desc(sfa, 0, 128, kSwizzleNone));
-          tc_cp_32x128b_warpx4(sf_col + 4, make_smem_desc(sfb, 0, 128, kSwizzleNone));
-          const uint32_t a_base = smem_u32(smem + C::kOffA + stage * C::kABytes);
-          const uint32_t b_base = smem_u32(smem + C::kOffB + stage * C::kBBytes);
+          for (int i = 0; i < nk; ++i) {
+            const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + 8 * (stage * kKBS + i));
+            const uint32_t sfa = smem_u32(smem + C::kOffSfa + (stage * kKBS + i) * 512);
+            const uint32_t sfb = smem_u32(smem + C::kOffSfb + (stage * kKBS + i) * 512);
+            tc_cp_32x128b_warpx4(sf_col, make_smem_desc(sfa, 0, 128, kSwizzleNone));
+            tc_cp_32x128b_warpx4(sf_col + 4, make_smem_desc(sfb, 0, 128, kSwizzleNone));
+            const uint32_t a_base = smem_u32(smem + C::kOffA + stage * C::kABytes + i * C::kATile);
+            const uint32_t b_base = smem_u32(smem + C::kOffB + stage * C::kBBytes + i * C::kBTile);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = make_smem_desc(a_base + kk * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bd = make_smem_desc(b_base + kk * 32, 16, 1024, kSwizzle128B);
-            tc_mma_mxf8f6f4(d_tmem, ad, bd, make_idesc_fp4w_fp8a(BN, kk), sf_col, sf_col + 4,
-                            (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = make_smem_desc(a_base + kk * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bd = make_smem_desc(b_base + kk * 32, 16, 1024, kSwizzle128B);
+              tc_mma_mxf8f6f4(d_tmem, ad, bd, make_idesc_fp4w_fp8a(n_mma, kk), sf_col, sf_col + 4,
+                              ((kb + i) | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&empty[stage]);
         }
@@ -305,25 +377,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
       const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
-      if (et < BN) {
-        int p = -1;
-        float wt = 0.f;
-        if (et < ti.valid) {
-          p = __ldg(args.perm + ti.s0 + et);
-          if (PHASE == 1) wt = __ldg(args.topk_w + p);
-        }
-        row_pair[et] = p;
-        row_w[et] = wt;
+      if (et < ti.valid) {
+        if (PHASE == 1) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
+        else row_pair[et] = __ldg(args.perm + ti.s0 + et);
       }
       // the four epilogue warps agree on the outcome of the bounded wait before
       // any of them enters another named barrier
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&tmem_full[acc], acc_phase, status, kWaitLimit, kWaitEpiTmemFull, w));
+      const bool got = __all_sync(0xffffffffu,
+                                  MXQ_TIMED_WAIT(3, mbar_wait(&tmem_full[acc], acc_phase, status, kWaitLimit, kWaitEpiTmemFull, w)));
       if (lane == 0) vote[q] = got ? 1 : 0;
       named_bar_sync(1, kEpiThreads);
       if (!(vote[0] & vote[1] & vote[2] & vote[3])) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      for (int c0 = 0; c0 < BN; c0 += kChunk) {
+      for (int c0 = 0; c0 < ti.valid; c0 += kChunk) {
         uint32_t v[16];
         tmem_ld_32x32b_x16(t_row + (uint32_t)c0, v);
         tmem_ld_wait();
@@ -349,21 +416,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
           for (int it = q; it < 2 * kChunk; it += 4) {
             const int col = it >> 1, grp = it & 1;
+            const int c = c0 + col;
+            if (c >= ti.valid) continue;                              // warp-uniform
             const float h = ebuf_f[col * 64 + grp * 32 + lane];
             const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
             const int e = ue8m0_exponent<true>(__uint_as_float(amax_bits));
             const uint8_t code = (uint8_t)(cvt_e4m3x2(h * pow2_neg(e), 0.f) & 0xFFu);
-            const int c = c0 + col;
-            if (c < ti.valid) {
-              const size_t s = (size_t)(ti.s0 + c);
-              const int fcol = ti.mt * 64 + grp * 32;                // first feature of the group
-              args.hq[s * args.I + fcol + lane] = code;
-              if (lane == 0) {
-                const int fg = fcol >> 5;                             // 32-group index along I
-                const size_t chunk = (size_t)ti.g * (args.I / 128) + (fg >> 2);
-                args.sfb2[chunk * 512 + (c & 31) * 16 + (c >> 5) * 4 + (fg & 3)] = (uint8_t)(e + 127);
-                if (args.hs_out) args.hs_out[s * (args.I / 32) + fg] = (uint8_t)(e + 127);
-              }
+            const size_t s = (size_t)(ti.s0 + c);
+            const int fcol = ti.mt * 64 + grp * 32;                  // first feature of the group
+            args.hq[s * args.I + fcol + lane] = code;
+            if (lane == 0) {
+              const int fg = fcol >> 5;                               // 32-group index along I
+              const size_t chunk = (size_t)ti.g * (args.I / 128) + (fg >> 2);
+              args.sfb2[chunk * 512 + (c & 31) * 16 + (c >> 5) * 4 + (fg & 3)] = (uint8_t)(e + 127);
+              if (args.hs_out) args.hs_out[s * (args.I / 32) + fg] = (uint8_t)(e + 127);
             }
           }
           named_bar_sync(1, kEpiThreads);
@@ -396,6 +462,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (acc == 0) acc_phase ^= 1;
     }
   }
+#ifdef MOE_MXQ_WAIT_STATS
+  if (lane == 0) {
+    unsigned long long *acc64 = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(status) + 64);
+    for (int i = 0; i < 4; ++i)
+      if (wait_acc[i]) atomicAdd(acc64 + i, (unsigned long long)wait_acc[i]);
+    if (warp <= 2) atomicAdd(acc64 + 4 + warp, (unsigned long long)(clock64() - k_t0));
+    if (warp == 0) {
+      for (int w = blockIdx.x; w < total_work; w += gridDim.x) ++n_items;
+      atomicAdd(acc64 + 7, (unsigned long long)n_items);
+    }
+  }
+#endif
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -404,20 +482,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Scale chunks of a GEMM's token operand.  For pool row s (tile g, row r)
-// copy the 4 scale bytes of K block kb into chunk (g, kb) at byte
-// (r%32)*16 + (r/32)*4.  GEMM1 takes them from the activation scales of token
-// perm[s]/k (FROM_TOKENS); GEMM2 fed with an external h takes them from row s
-// of that h's scales.
+// Per pool row s (expert e, tile g = tile_off[e] + rank/BN, row r = rank%BN):
+//   FROM_TOKENS (before GEMM1): token t = perm[s]/k -> tok_pool[s], its top-k
+//     weight -> w_pool[s], the 4 scale bytes of each K block of xs[t] into
+//     chunk (g, kb) at byte (r%32)*16 + (r/32)*4, and (large token tiles) the
+//     FP8 row xq[t] -> xq_pool[s];
+//   otherwise (GEMM2 fed with an external h): the scale bytes of row s of
+//     that h into GEMM2's chunks.
 template <int BN, bool FROM_TOKENS>
-__global__ void __launch_bounds__(256) prep_scale_chunks_kernel(const uint8_t *__restrict__ src_scales,
-                                                                const int32_t *__restrict__ counts,
-                                                                const int32_t *__restrict__ offsets,
-                                                                const int32_t *__restrict__ perm, int E, int k,
-                                                                int KB, uint8_t *__restrict__ chunks) {
+__global__ void __launch_bounds__(256) prep_pool_kernel(const uint8_t *__restrict__ src_scales,
+                                                        const int32_t *__restrict__ counts,
+                                                        const int32_t *__restrict__ offsets,
+                                                        const int32_t *__restrict__ perm,
+                                                        const float *__restrict__ topk_w, int E, int k, int KB,
+                                                        uint8_t *__restrict__ chunks, int32_t *__restrict__ tok_pool,
+                                                        float *__restrict__ w_pool, const uint4 *__restrict__ xq,
+                                                        uint4 *__restrict__ xq_pool, int row16) {
   extern __shared__ int sh[];
   int *tile_off = sh, *cnt_sm = sh + (E + 1), *off_sm = sh + 2 * (E + 1);
-  if (threadIdx.x < 32) build_tile_map<BN>(counts, offsets, E, tile_off, cnt_sm, off_sm);
+  load_expert_table(counts, offsets, E, cnt_sm, off_sm);
+  __syncthreads();
+  if (threadIdx.x < 32) scan_tile_map<BN>(cnt_sm, E, tile_off);
   __syncthreads();
   const int P = off_sm[E];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -430,7 +515,20 @@ __global__ void __launch_bounds__(256) prep_scale_chunks_kernel(const uint8_t *_
     }
     const int rank = s - off_sm[lo];
     const int g = tile_off[lo] + rank / BN, r = rank % BN;
-    const int row = FROM_TOKENS ? __ldg(perm + s) / k : s;
+    int row = s;
+    if (FROM_TOKENS) {
+      const int p = __ldg(perm + s);
+      row = p / k;
+      if (lane == 0) {
+        tok_pool[s] = row;
+        w_pool[s] = __ldg(topk_w + p);
+      }
+      if (xq_pool) {
+        const uint4 *src = xq + (size_t)row * row16;
+        uint4 *dst = xq_pool + (size_t)s * row16;
+        for (int i = lane; i < row16; i += 32) dst[i] = __ldg(src + i);
+      }
+    }
     const uint32_t *src = reinterpret_cast<const uint32_t *>(src_scales + (size_t)row * KB * 4);
     for (int kb = lane; kb < KB; kb += 32) {
       const uint32_t wv = __ldg(src + kb);
@@ -440,67 +538,79 @@ __global__ void __launch_bounds__(256) prep_scale_chunks_kernel(const uint8_t *_
 }
 
 template <int BN, bool FROM_TOKENS>
-int launch_prep(const uint8_t *src, const moe_expert_args *a, int KB, uint8_t *chunks, cudaStream_t st) {
+int launch_prep(const uint8_t *src, const moe_expert_args *a, int KB, uint8_t *chunks, int32_t *tok_pool,
+                float *w_pool, uint8_t *xq_pool, cudaStream_t st) {
   const int64_t P = a->T * a->k;
   const size_t sm = (size_t)3 * (a->E + 1) * 4;
   const int64_t blocks = ceil_div(P, 8);
   const int cap = num_sms() * 4;
   const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
-  prep_scale_chunks_kernel<BN, FROM_TOKENS><<<grid, 256, sm, st>>>(src, a->counts, a->offsets, a->perm, a->E, a->k,
-                                                                   KB, chunks);
+  prep_pool_kernel<BN, FROM_TOKENS><<<grid, 256, sm, st>>>(
+      src, a->counts, a->offsets, a->perm, a->topk_w, a->E, a->k, KB, chunks, tok_pool, w_pool,
+      reinterpret_cast<const uint4 *>(a->xq), reinterpret_cast<uint4 *>(xq_pool), (int)(a->H / 16));
   return launch_status();
 }
 
 template <int BN>
 int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &lay, cudaStream_t st) {
+  using C = Cfg<BN>;
   uint8_t *sfb1 = reinterpret_cast<uint8_t *>(ws + lay.sfb1);
   uint8_t *sfb2 = reinterpret_cast<uint8_t *>(ws + lay.sfb2);
   uint8_t *hq = a->hq ? a->hq : reinterpret_cast<uint8_t *>(ws + lay.hq);
+  int32_t *tok_pool = reinterpret_cast<int32_t *>(ws + lay.tok_pool);
+  float *w_pool = reinterpret_cast<float *>(ws + lay.w_pool);
+  uint8_t *xq_pool = reinterpret_cast<uint8_t *>(ws + lay.xq_pool);
   const int64_t P = a->T * a->k;
   const int E = a->E;
   const int phases = a->phases ? a->phases : (MOE_PHASE_TOKEN_SCALES | MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2);
 
-  // token-scale chunks of GEMM1 (gathered by pair id)
+  // pool rows of GEMM1: token ids, weights, token-scale chunks (+ FP8 rows for large tiles)
   if ((phases & MOE_PHASE_TOKEN_SCALES) &&
-      launch_prep<BN, true>(a->xs, a, (int)(a->H / 128), sfb1, st) != MOE_OK)
+      launch_prep<BN, true>(a->xs, a, (int)(a->H / 128), sfb1, tok_pool, w_pool, xq_pool, st) != MOE_OK)
     return MOE_ERR_CUDA;
   // scale chunks of GEMM2 from a caller-provided h (instead of GEMM1's epilogue)
-  if ((phases & MOE_PHASE_H_SCALES) && launch_prep<BN, false>(a->hs, a, (int)(a->I / 128), sfb2, st) != MOE_OK)
+  if ((phases & MOE_PHASE_H_SCALES) &&
+      launch_prep<BN, false>(a->hs, a, (int)(a->I / 128), sfb2, nullptr, nullptr, nullptr, st) != MOE_OK)
     return MOE_ERR_CUDA;
 
   GemmArgs g{};
   g.E = E; g.k = a->k; g.T = (int)a->T; g.H = (int)a->H; g.I = (int)a->I;
-  g.counts = a->counts; g.offsets = a->offsets; g.perm = a->perm; g.topk_w = a->topk_w;
+  g.counts = a->counts; g.offsets = a->offsets; g.perm = a->perm;
+  g.tok_pool = tok_pool; g.w_pool = w_pool;
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
   const size_t sm = smem_bytes<BN>(E);
   const int grid = num_sms();
+  g.prefetch_stages = C::kDefaultPrefetchStages;
+  if (const char *env = getenv("MOE_MXQ_PREFETCH_STAGES")) g.prefetch_stages = atoi(env);
 
   if (phases & MOE_PHASE_GEMM1) {
     // GEMM1 + SwiGLU (.) weight + FP8 requantisation
-    CUtensorMap tw1, tx;
-    bool ok = encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, (uint64_t)a->H,
-                             (uint64_t)E * 2 * a->I, (uint64_t)a->H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a->xq, (uint64_t)a->H, (uint64_t)a->T,
-                              (uint64_t)a->H, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t wrows = (uint64_t)E * (2 * a->I / 128) * (a->H / 128) * 128;
+    CUtensorMap tw1, tb;
+    bool ok = encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, 128, wrows, 64, 128,
+                             kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)xq_pool, (uint64_t)a->H, (uint64_t)P,
+                              (uint64_t)a->H, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
     g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
-    g.w_sf = a->w1s; g.b_sf = sfb1;
+    g.w_codes = a->w1q; g.w_sf = a->w1s; g.b_sf = sfb1;
     if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
-    expert_gemm_kernel<BN, 1><<<grid, kThreads, sm, st>>>(tw1, tx, g);
+    expert_gemm_kernel<BN, 1><<<grid, kThreads, sm, st>>>(tw1, tb, g);
     if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
   }
   if (phases & MOE_PHASE_GEMM2) {
     // GEMM2 -> BF16 per pair
+    const uint64_t wrows = (uint64_t)E * (a->H / 128) * (a->I / 128) * 128;
     CUtensorMap tw2, th;
-    bool ok = encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, (uint64_t)a->I,
-                             (uint64_t)E * a->H, (uint64_t)a->I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    bool ok = encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, 128, wrows, 64, 128,
+                             kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
                               (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
     g.M = (int)a->H; g.K = (int)a->I; g.KB = (int)(a->I / 128); g.MT = (int)(a->H / 128);
-    g.w_sf = a->w2s; g.b_sf = sfb2;
+    g.w_codes = a->w2q; g.w_sf = a->w2s; g.b_sf = sfb2;
     g.hs_out = nullptr;
     if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
         cudaSuccess)

@@ -36,6 +36,9 @@ struct ExpertWs {
   size_t sfb1;       // GEMM1 token-scale chunks [max_tiles][H/128][512]
   size_t sfb2;       // GEMM2 token-scale chunks [max_tiles][I/128][512]
   size_t hq;         // requantised h in pool order [P][I]
+  size_t tok_pool;   // token index of each pool row [P]
+  size_t w_pool;     // top-k weight of each pool row [P]
+  size_t xq_pool;    // FP8 activations in pool order [P][H] (large token tiles)
   size_t total;
 };
 
@@ -52,6 +55,9 @@ inline ExpertWs expert_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int
   w.sfb1 = off;    off += round_up((size_t)tiles * (size_t)(H / 128) * 512, 256);
   w.sfb2 = off;    off += round_up((size_t)tiles * (size_t)(I / 128) * 512, 256);
   w.hq = off;      off += round_up((size_t)P * (size_t)I, 256);
+  w.tok_pool = off; off += round_up((size_t)P * 4, 256);
+  w.w_pool = off;  off += round_up((size_t)P * 4, 256);
+  w.xq_pool = off; off += round_up((size_t)P * (size_t)H, 256);
   w.total = off;
   return w;
 }

@@ -59,8 +59,11 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const uint4 *__rest
 }
 
 // Weight quantisation.  Row n of group g in the input (K values) is written
-// to stored row dst_row(n); scales go either row-major [G][N][K/32] or to the
-// MMA chunk layout [G][N/128][K/128][512] (byte (r%32)*16 + (r/32)*4 + kk).
+// to stored row r (the gate/up interleave for MMA_L1).  Canonical: codes
+// row-major [G][N][K/2], scales [G][N][K/32].  MMA layouts: codes in
+// tile-contiguous blocks [G][N/128][K/128][128 rows][64 bytes] (one 128 x 128
+// tile = 8 KB in one piece) and scales in chunks [G][N/128][K/128][512] with
+// byte (r%32)*16 + (r/32)*4 + kk.
 __global__ void __launch_bounds__(kThreads) quant_weight_kernel(const uint4 *__restrict__ w, int64_t G,
                                                                 int64_t N, int64_t K, int layout,
                                                                 uint32_t *__restrict__ q,
@@ -97,7 +100,13 @@ __global__ void __launch_bounds__(kThreads) quant_weight_kernel(const uint4 *__r
       const int64_t f_idx = up ? n - half : n;
       r = (f_idx >> 3) * 16 + (up ? 8 : 0) + (f_idx & 7);
     }
-    q[(g * N + r) * items_per_row + col_item] = packed;
+    if (layout == MXQ_LAYOUT_CANONICAL) {
+      q[(g * N + r) * items_per_row + col_item] = packed;
+    } else {
+      // tile-contiguous: [g][r/128][k/128][r%128][64 bytes]; 16 words of 4 bytes per tile row
+      const int64_t nt = r >> 7, rr = r & 127, kb = col_item >> 4, w16 = col_item & 15;
+      q[(((g * (N / 128) + nt) * (K / 128) + kb) * 128 + rr) * 16 + w16] = packed;
+    }
     if ((col_item & 3) == 0) {
       const int64_t kg = col_item >> 2;           // 32-group along K
       int64_t off;

@@ -60,11 +60,13 @@ def canonical_to_mma(q: np.ndarray, s: np.ndarray, interleave: bool):
     pos = (rr % 32) * 16 + (rr // 32) * 4             # [rr]
     for kk in range(4):
         chunk[:, :, :, pos + kk] = sc[:, :, :, :, kk].transpose(0, 1, 3, 2)
-    return np.ascontiguousarray(q), chunk.reshape(-1)
+    qt = q.reshape(G, NT, 128, KB, 64).transpose(0, 1, 3, 2, 4)        # [g, nt, kb, row, 64 B]
+    return np.ascontiguousarray(qt).reshape(G, N, K2), chunk.reshape(-1)
 
 
 def mma_to_canonical(q: np.ndarray, chunk: np.ndarray, G: int, N: int, K: int, interleave: bool):
     NT, KB = N // 128, K // 128
+    q = np.ascontiguousarray(q.reshape(G, NT, KB, 128, 64).transpose(0, 1, 3, 2, 4)).reshape(G, N, K // 2)
     c = chunk.reshape(G, NT, KB, 512)
     rr = np.arange(128)
     pos = (rr % 32) * 16 + (rr // 32) * 4
