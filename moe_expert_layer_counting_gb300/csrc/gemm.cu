@@ -59,15 +59,20 @@ constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in H
 // decode-sized tiles streaming.
 constexpr int kKBS = 2;
 
+// Small token tiles run two CTAs per SM (each with half the shared memory):
+// with N <= 32 the MMA issuer, not the tensor core, limits a CTA, and two
+// CTAs give the SM two independent MMA issue streams.
 template <int BN>
 struct Cfg {
+  static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
   static constexpr int kATile = kBM * kBK;                  // one unpacked FP4 tile (8-bit containers)
   static constexpr int kBTile = BN * kBK;
   static constexpr int kABytes = kKBS * kATile;
   static constexpr int kBBytes = kKBS * kBTile;
   static constexpr int kSfbBytes = (BN < 32 ? BN : 32) * 16; // used bytes of a token-scale chunk
   static constexpr int kStageBytes = kABytes + kBBytes + kKBS * 1024;
-  static constexpr int kStages = (200 * 1024 / kStageBytes) > 8 ? 8 : (200 * 1024 / kStageBytes);
+  static constexpr int kSmemBudget = (kCtasPerSm == 1 ? 200 : 96) * 1024;
+  static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
   static constexpr int kTmemCols = 2 * BN + 8 * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                          : kTmemCols <= 256 ? 256 : 512;
@@ -184,7 +189,7 @@ __device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int 
 #endif
 
 template <int BN, int PHASE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                        const GemmArgs args) {
   using C = Cfg<BN>;
@@ -579,7 +584,7 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   g.tok_pool = tok_pool; g.w_pool = w_pool;
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
   const size_t sm = smem_bytes<BN>(E);
-  const int grid = num_sms();
+  const int grid = num_sms() * C::kCtasPerSm;
   g.prefetch_stages = C::kDefaultPrefetchStages;
   if (const char *env = getenv("MOE_MXQ_PREFETCH_STAGES")) g.prefetch_stages = atoi(env);
 
