@@ -33,6 +33,7 @@
 // tiles of one expert) or a token tile (weight tiles of one expert) in L2.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdlib>
 
 #include "host_common.h"
@@ -51,20 +52,19 @@ constexpr long long kWaitLimit = 2000000000LL;
 constexpr int kMaxE = 1024;
 constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in HBM (8 KB)
 
-// A pipeline stage covers kKBS K blocks of 128 (256 K): one TMA box of 256
-// weight rows (two consecutive tiles of the tile-contiguous layout), one bulk
-// copy per scale operand and one 2-D box of token rows per K block.  Every
-// asynchronous instruction costs tens of issue cycles in the producer and MMA
-// warps, so fewer, larger copies per byte of weights is what keeps
-// decode-sized tiles streaming.
-constexpr int kKBS = 2;
-
-// Small token tiles run two CTAs per SM (each with half the shared memory):
-// with N <= 32 the MMA issuer, not the tensor core, limits a CTA, and two
-// CTAs give the SM two independent MMA issue streams.
+// Issue cost.  Every asynchronous instruction (TMA copy, tcgen05.cp,
+// tcgen05.mma) takes ~80 cycles of its issuing thread, whatever its size,
+// while one M=128 x N x K=32 MMA keeps the tensor core busy ~0.53 N cycles.
+// So (a) a pipeline stage of a decode-sized tile covers kKBS = 2 K blocks:
+// one TMA box of 256 weight rows (two consecutive tiles of the
+// tile-contiguous layout), one bulk copy per scale operand and one 2-D box of
+// token rows per K block; and (b) tiles up to N = 64 run two CTAs per SM
+// (half the shared memory each), giving the SM two independent MMA issue
+// streams without changing any accumulation order.
 template <int BN>
 struct Cfg {
-  static constexpr int kCtasPerSm = BN <= 32 ? 2 : 1;
+  static constexpr int kKBS = BN == 64 ? 1 : 2;
+  static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
   static constexpr int kATile = kBM * kBK;                  // one unpacked FP4 tile (8-bit containers)
   static constexpr int kBTile = BN * kBK;
   static constexpr int kABytes = kKBS * kATile;
@@ -76,8 +76,10 @@ struct Cfg {
   static constexpr int kTmemCols = 2 * BN + 8 * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                          : kTmemCols <= 256 ? 256 : 512;
-  // decode-sized tiles: optional L2 prefetch distance (stages) of weight tiles
-  static constexpr int kDefaultPrefetchStages = 0;
+  // decode-sized tiles: the weights of the next kPrefetchItems work items of
+  // a CTA are requested into L2 ahead of their TMA loads (a few bulk
+  // prefetches per work item: its tiles are contiguous in HBM)
+  static constexpr int kDefaultPrefetchItems = 0;
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -100,7 +102,8 @@ size_t smem_bytes(int E) {
 struct GemmArgs {
   int E, k, T, H, I;
   int M, K, KB, MT;                 // weight rows / reduction / K blocks / weight tiles per expert
-  int prefetch_stages;              // L2 prefetch distance of weight tiles, in stages (0 = off)
+  int prefetch_items;               // L2 prefetch distance of weight tiles, in work items (0 = off)
+  uint32_t prefetch_bytes;          // bytes of codes prefetched per work item
   const int32_t *counts, *offsets, *perm;
   const int32_t *tok_pool;          // token of each pool row (GEMM1 gather)
   const float *w_pool;              // top-k weight of each pool row (GEMM1 epilogue)
@@ -255,39 +258,28 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;
     bool ok = true;
-    // L2 prefetch cursor over this CTA's (work item, K block) sequence; it runs
-    // kPrefetchStages stages ahead of the loads (decode-sized tiles only).
-    int pf_w = blockIdx.x, pf_kb = 0;
-    TileInfo pf_ti{};
-    const int pf_dist = args.prefetch_stages;
-    if (pf_dist > 0 && pf_w < total_work)
-      pf_ti = decode_work<BN>(pf_w, args.MT, args.E, tile_off, cnt_sm, off_sm);
-    auto pf_step = [&](bool issue) {
-      if (pf_w >= total_work) return;
-      const int nk = min(kKBS, args.KB - pf_kb);
-      if (issue && lane == 0) {
-        const size_t t = ((size_t)(pf_ti.e * args.MT + pf_ti.mt) * args.KB + pf_kb);
-        prefetch_l2_bulk(args.w_codes + t * kWTileBytes, nk * kWTileBytes);
-        prefetch_l2_bulk(args.w_sf + t * 512, nk * 512);
-      }
-      pf_kb += nk;
-      if (pf_kb == args.KB) {
-        pf_kb = 0;
-        pf_w += gridDim.x;
-        if (pf_w < total_work) pf_ti = decode_work<BN>(pf_w, args.MT, args.E, tile_off, cnt_sm, off_sm);
-      }
+    // L2 prefetch of whole work items (codes and scales of all K blocks),
+    // kept prefetch_items items ahead of the item being loaded.
+    const int pf_items = args.prefetch_items;
+    auto prefetch_item = [&](int w) {
+      if (w >= total_work || lane != 0) return;
+      const TileInfo t = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      const size_t first = (size_t)(t.e * args.MT + t.mt) * args.KB;
+      const uint8_t *codes = args.w_codes + first * kWTileBytes;
+      const uint32_t code_bytes = min((uint32_t)args.KB * kWTileBytes, args.prefetch_bytes);
+      for (uint32_t off = 0; off < code_bytes; off += 65536u)
+        prefetch_l2_bulk(codes + off, min(65536u, code_bytes - off));
+      prefetch_l2_bulk(args.w_sf + first * 512, (uint32_t)args.KB * 512);
     };
-    if (pf_dist > 0) {
-      for (int i = 0; i < C::kStages; ++i) pf_step(false);        // those go straight to shared memory
-      for (int i = 0; i < pf_dist; ++i) pf_step(true);
-    }
+    for (int i = 0; i <= pf_items && pf_items > 0; ++i) prefetch_item(blockIdx.x + i * gridDim.x);
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
       const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      if (pf_items > 0 && w != (int)blockIdx.x) prefetch_item(w + pf_items * (int)gridDim.x);
       const int wtile = (ti.e * args.MT + ti.mt) * args.KB;        // first weight tile of this item
       const uint8_t *sfa_src = args.w_sf + (size_t)wtile * 512;
       const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB) * 512;
-      for (int kb = 0; kb < args.KB; kb += kKBS) {
-        const int nk = min(kKBS, args.KB - kb);                   // K blocks in this stage
+      for (int kb = 0; kb < args.KB; kb += C::kKBS) {
+        const int nk = min(C::kKBS, args.KB - kb);                   // K blocks in this stage
         if (!__all_sync(0xffffffffu,
                         MXQ_TIMED_WAIT(0, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb)))) {
           ok = false;
@@ -299,15 +291,14 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
           // the weight box always spans kKBS tiles (rows past the tensor read as zeros);
           // the FP4-unpacking load completes the packed byte count
           const uint32_t sfb_bytes = (uint32_t)((nk - 1) * 512 + C::kSfbBytes);
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(kKBS * kWTileBytes + nk * C::kBTile + nk * 512) + sfb_bytes);
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(C::kKBS * kWTileBytes + nk * C::kBTile + nk * 512) + sfb_bytes);
           tma_load_2d(a_dst, &tmap_w, &full[stage], 0, (wtile + kb) * kBM);
-          bulk_load(smem + C::kOffSfa + stage * kKBS * 512, sfa_src + (size_t)kb * 512, nk * 512, &full[stage]);
-          bulk_load(smem + C::kOffSfb + stage * kKBS * 512, sfb_src + (size_t)kb * 512, sfb_bytes, &full[stage]);
+          bulk_load(smem + C::kOffSfa + stage * C::kKBS * 512, sfa_src + (size_t)kb * 512, nk * 512, &full[stage]);
+          bulk_load(smem + C::kOffSfb + stage * C::kKBS * 512, sfb_src + (size_t)kb * 512, sfb_bytes, &full[stage]);
           for (int i = 0; i < nk; ++i)
             tma_load_2d(b_dst + i * C::kBTile, &tmap_b, &full[stage], (kb + i) * kBK, ti.s0);
         }
         __syncwarp();
-        if (pf_dist > 0) pf_step(true);
         issued_mask |= 1u << stage;
         issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -333,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
         break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < args.KB; kb += kKBS) {
-        const int nk = min(kKBS, args.KB - kb);
+      for (int kb = 0; kb < args.KB; kb += C::kKBS) {
+        const int nk = min(C::kKBS, args.KB - kb);
         if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(1, mbar_wait(&full[stage], phase, status, kWaitLimit, kWaitMmaFull, kb)))) {
           ok = false;
           break;
@@ -342,9 +333,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
         tc_fence_after();
         if (lane == 0) {
           for (int i = 0; i < nk; ++i) {
-            const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + 8 * (stage * kKBS + i));
-            const uint32_t sfa = smem_u32(smem + C::kOffSfa + (stage * kKBS + i) * 512);
-            const uint32_t sfb = smem_u32(smem + C::kOffSfb + (stage * kKBS + i) * 512);
+            const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + 8 * (stage * C::kKBS + i));
+            const uint32_t sfa = smem_u32(smem + C::kOffSfa + (stage * C::kKBS + i) * 512);
+            const uint32_t sfb = smem_u32(smem + C::kOffSfb + (stage * C::kKBS + i) * 512);
             tc_cp_32x128b_warpx4(sf_col, make_smem_desc(sfa, 0, 128, kSwizzleNone));
             tc_cp_32x128b_warpx4(sf_col + 4, make_smem_desc(sfb, 0, 128, kSwizzleNone));
             const uint32_t a_base = smem_u32(smem + C::kOffA + stage * C::kABytes + i * C::kATile);
@@ -585,20 +576,29 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
   const size_t sm = smem_bytes<BN>(E);
   const int grid = num_sms() * C::kCtasPerSm;
-  g.prefetch_stages = C::kDefaultPrefetchStages;
-  if (const char *env = getenv("MOE_MXQ_PREFETCH_STAGES")) g.prefetch_stages = atoi(env);
+  // L2 budget for prefetched weights: ~64 MB over the grid, one or two items ahead
+  const auto set_prefetch = [&](int64_t KB) {
+    const int64_t item = KB * (kWTileBytes + 512);
+    const int64_t budget = (64ll << 20) / grid;
+    int items = C::kDefaultPrefetchItems;
+    if (const char *env = getenv("MOE_MXQ_PREFETCH_ITEMS")) items = atoi(env);
+    if (items > 0) items = (int)std::max<int64_t>(1, std::min<int64_t>(items, budget / item));
+    g.prefetch_items = items;
+    g.prefetch_bytes = (uint32_t)std::min<int64_t>(KB * kWTileBytes, items > 0 ? budget / items : 0) & ~15u;
+  };
 
   if (phases & MOE_PHASE_GEMM1) {
     // GEMM1 + SwiGLU (.) weight + FP8 requantisation
     const uint64_t wrows = (uint64_t)E * (2 * a->I / 128) * (a->H / 128) * 128;
     CUtensorMap tw1, tb;
     bool ok = encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, 128, wrows, 64, 128,
-                             kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+                             C::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)xq_pool, (uint64_t)a->H, (uint64_t)P,
                               (uint64_t)a->H, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
     g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
     g.w_codes = a->w1q; g.w_sf = a->w1s; g.b_sf = sfb1;
+    set_prefetch(g.KB);
     if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
@@ -610,12 +610,13 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     const uint64_t wrows = (uint64_t)E * (a->H / 128) * (a->I / 128) * 128;
     CUtensorMap tw2, th;
     bool ok = encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, 128, wrows, 64, 128,
-                             kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+                             C::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
                               (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
     g.M = (int)a->H; g.K = (int)a->I; g.KB = (int)(a->I / 128); g.MT = (int)(a->H / 128);
     g.w_codes = a->w2q; g.w_sf = a->w2s; g.b_sf = sfb2;
+    set_prefetch(g.KB);
     g.hs_out = nullptr;
     if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
         cudaSuccess)

@@ -65,13 +65,14 @@ inline ExpertWs expert_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int
 // Every public workspace starts with this many bytes of status words.
 constexpr size_t kStatusBytes = 256;
 
-// Token tile chosen from the mean number of pairs per routed expert.
+// Token tile chosen from the mean number of pairs per routed expert (tiles up
+// to 64 run two CTAs per SM; 128 only pays off for heavily loaded experts).
 inline int choose_tile_n(int64_t P, int64_t E) {
   const int64_t ne = E < P ? E : P;
   const int64_t mean = ne > 0 ? ceil_div(P, ne) : 1;
   if (mean <= 16) return 16;
   if (mean <= 32) return 32;
-  if (mean <= 64) return 64;
+  if (mean <= 192) return 64;
   return 128;
 }
 
