@@ -65,6 +65,9 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uin
 
 namespace {
 
+// moe_forward casts x straight into pool order when P * H is at most this
+constexpr int64_t kPoolCastMaxValues = int64_t(16) << 20;
+
 struct ForwardWs {
   size_t xq, xs, idx, w, counts, offsets, perm, inv_perm, perm_scratch, expert, y_pairs, total;
 };
@@ -108,7 +111,6 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   if (a->workspace_bytes < lay.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   char *ws = reinterpret_cast<char *>(a->workspace);
   int *status = reinterpret_cast<int *>(ws);
-  const int64_t P = a->T * a->k;
 
   moe_expert_args ea{};
   ea.struct_size = sizeof(moe_expert_args);
@@ -142,16 +144,28 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  rc = launch_quant_act(a->x, a->T, a->H, const_cast<uint8_t *>(ea.xq), const_cast<uint8_t *>(ea.xs), st);
-  if (rc != MOE_OK) return rc;
   rc = launch_route(a->logits, a->T, a->E, a->k, idx, wts, st);
   if (rc != MOE_OK) return rc;
+  const int64_t P = a->T * a->k;
   rc = launch_permute(idx, a->T, a->E, a->k, counts, offsets, perm, reinterpret_cast<int32_t *>(ws + lay.inv_perm),
                       status, ws + lay.perm_scratch, st);
   if (rc != MOE_OK) return rc;
+  ea.tile_n = a->tile_n ? a->tile_n : choose_tile_n(P, a->E);
+  if (P * a->H <= kPoolCastMaxValues) {
+    // small problems: cast x straight into GEMM1's pool rows and scale chunks
+    // (one launch, every load in flight at once)
+    rc = launch_pool_cast(&ea, a->x, ws + lay.expert, st);
+    if (rc != MOE_OK) return rc;
+    ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
+  } else {
+    // large problems: cast each token once, then copy FP8 rows into pool order
+    // (half the bytes of re-reading BF16 rows k times)
+    rc = launch_quant_act(a->x, a->T, a->H, const_cast<uint8_t *>(ea.xq), const_cast<uint8_t *>(ea.xs), st);
+    if (rc != MOE_OK) return rc;
+    ea.phases = 0;
+  }
   rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
   if (rc != MOE_OK) return rc;
-  (void)P;
   return launch_combine(ea.y_pairs, idx, a->T, a->k, a->H, a->y, st);
 }
 

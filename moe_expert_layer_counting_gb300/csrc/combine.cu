@@ -20,6 +20,8 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4 *__restrict__ yp,
                                                            const int32_t *__restrict__ idx, int64_t T, int k,
                                                            int64_t H8, uint4 *__restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t items = T * H8;
   const int64_t slot_stride = T * H8;        // uint4 elements between slots
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
@@ -54,9 +56,8 @@ int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k
   const int64_t items = T * (H / 8);
   const int64_t blocks = ceil_div(items, kThreads);
   const int64_t cap = (int64_t)num_sms() * 8;
-  combine_kernel<<<(int)(blocks < cap ? blocks : cap), kThreads, 0, st>>>(
-      reinterpret_cast<const uint4 *>(y_pairs), idx, T, k, H / 8, reinterpret_cast<uint4 *>(y));
-  return launch_status();
+  return launch_pdl(combine_kernel, dim3((int)(blocks < cap ? blocks : cap)), dim3(kThreads), 0, st,
+                    reinterpret_cast<const uint4 *>(y_pairs), idx, T, k, H / 8, reinterpret_cast<uint4 *>(y));
 }
 
 }  // namespace mxq

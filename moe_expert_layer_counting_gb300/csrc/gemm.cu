@@ -45,8 +45,6 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 128;
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
 constexpr int kChunk = 16;                    // accumulator columns per epilogue step
 constexpr long long kWaitLimit = 2000000000LL;
 constexpr int kMaxE = 1024;
@@ -63,17 +61,25 @@ constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in H
 // streams without changing any accumulation order.
 template <int BN>
 struct Cfg {
-  static constexpr int kKBS = BN == 64 ? 1 : 2;
+  // tiles above 128 tokens: one K block per stage, scales of the token operand
+  // in two 128-row groups, and an 8-warp epilogue (two warps per TMEM quadrant)
+  static constexpr int kKBS = (BN == 64 || BN > 128) ? 1 : 2;
   static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
+  static constexpr int kSfbGroups = (BN + 127) / 128;       // 128-row groups of token scales
+  static constexpr int kTokChunk = 512 * kSfbGroups;        // bytes of one (tile, K block) token-scale chunk
+  static constexpr int kSfSlot = 4 + 4 * kSfbGroups;        // TMEM columns of one K block's scales
+  static constexpr int kEpiWarps = BN > 128 ? 8 : 4;
+  static constexpr int kEpiHalves = kEpiWarps / 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kATile = kBM * kBK;                  // one unpacked FP4 tile (8-bit containers)
   static constexpr int kBTile = BN * kBK;
   static constexpr int kABytes = kKBS * kATile;
   static constexpr int kBBytes = kKBS * kBTile;
-  static constexpr int kSfbBytes = (BN < 32 ? BN : 32) * 16; // used bytes of a token-scale chunk
-  static constexpr int kStageBytes = kABytes + kBBytes + kKBS * 1024;
+  static constexpr int kSfbBytes = BN < 32 ? BN * 16 : kTokChunk;   // used bytes of a token-scale chunk
+  static constexpr int kStageBytes = kABytes + kBBytes + kKBS * (512 + kTokChunk);
   static constexpr int kSmemBudget = (kCtasPerSm == 1 ? 200 : 96) * 1024;
   static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
-  static constexpr int kTmemCols = 2 * BN + 8 * kKBS * kStages;
+  static constexpr int kTmemCols = 2 * BN + kSfSlot * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                          : kTmemCols <= 256 ? 256 : 512;
   // decode-sized tiles: the weights of the next kPrefetchItems work items of
@@ -85,13 +91,15 @@ struct Cfg {
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kKBS * 512;
-  static constexpr int kOffEpi = kOffSfb + kStages * kKBS * 512;   // 4 KB epilogue staging
-  static constexpr int kOffRow = kOffEpi + 4096;            // pair id [BN] + weight [BN]
-  static constexpr int kOffBar = kOffRow + 8 * BN;
+  static constexpr int kOffEpi = kOffSfb + kStages * kKBS * kTokChunk;   // 4 KB epilogue staging per half
+  // per-item row info, double-buffered by accumulator: pair id [2][BN], weight [2][BN]
+  static constexpr int kOffRow = kOffEpi + 4096 * kEpiHalves;
+  static constexpr int kOffBar = kOffRow + 16 * BN;
   static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
-  static constexpr int kOffExp = kOffTmemPtr + 32;          // tile_off, counts, offsets: 3*(E+1) ints
+  static constexpr int kOffExp = kOffTmemPtr + 64;          // tile_off, counts, offsets: 3*(E+1) ints
   static_assert(kStages >= 2, "need at least two stages");
+  static_assert(kTmemCols <= 512, "TMEM budget");
 };
 
 template <int BN>
@@ -192,7 +200,7 @@ __device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int 
 #endif
 
 template <int BN, int PHASE>
-__global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                        const GemmArgs args) {
   using C = Cfg<BN>;
@@ -206,12 +214,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
   uint64_t *tmem_empty = tmem_full + 2;
   uint64_t *mma_done = tmem_full + 4;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::kOffTmemPtr);
-  int *vote = reinterpret_cast<int *>(smem + C::kOffTmemPtr + 4);     // [4], one per epilogue warp
+  int *vote = reinterpret_cast<int *>(smem + C::kOffTmemPtr + 4);     // one per epilogue warp
   int *tile_off = reinterpret_cast<int *>(smem + C::kOffExp);
   int *cnt_sm = tile_off + (args.E + 1);
   int *off_sm = cnt_sm + (args.E + 1);
-  int32_t *row_pair = reinterpret_cast<int32_t *>(smem + C::kOffRow);
-  float *row_w = reinterpret_cast<float *>(smem + C::kOffRow + 4 * BN);
+  int32_t *row_pair_buf = reinterpret_cast<int32_t *>(smem + C::kOffRow);
+  float *row_w_buf = reinterpret_cast<float *>(smem + C::kOffRow + 8 * BN);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int *status = args.status;
@@ -221,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
   int n_items = 0;
 #endif
 
-  load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm);
+  pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
@@ -235,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       }
       for (int a = 0; a < 2; ++a) {
         mbar_init(&tmem_full[a], 1);
-        mbar_init(&tmem_empty[a], kEpiThreads / 32);
+        mbar_init(&tmem_empty[a], C::kEpiWarps);
       }
       mbar_init(mma_done, 1);
       fence_mbar_init();
@@ -244,6 +252,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     tmem_alloc(tmem_ptr, C::kTmemAlloc);
     tmem_relinquish();
   }
+  // everything above touches no global memory; the previous kernel's outputs
+  // (counts, offsets, pool rows, scales) are read only after this point
+  pdl_wait();
+  load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm);
   __syncthreads();
   if (warp == 0) scan_tile_map<BN>(cnt_sm, args.E, tile_off);
   tc_fence_before();
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
       if (pf_items > 0 && w != (int)blockIdx.x) prefetch_item(w + pf_items * (int)gridDim.x);
       const int wtile = (ti.e * args.MT + ti.mt) * args.KB;        // first weight tile of this item
       const uint8_t *sfa_src = args.w_sf + (size_t)wtile * 512;
-      const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB) * 512;
+      const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB) * C::kTokChunk;
       for (int kb = 0; kb < args.KB; kb += C::kKBS) {
         const int nk = min(C::kKBS, args.KB - kb);                   // K blocks in this stage
         if (!__all_sync(0xffffffffu,
@@ -290,11 +302,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
         if (lane == 0) {
           // the weight box always spans kKBS tiles (rows past the tensor read as zeros);
           // the FP4-unpacking load completes the packed byte count
-          const uint32_t sfb_bytes = (uint32_t)((nk - 1) * 512 + C::kSfbBytes);
+          const uint32_t sfb_bytes = (uint32_t)((nk - 1) * C::kTokChunk + C::kSfbBytes);
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(C::kKBS * kWTileBytes + nk * C::kBTile + nk * 512) + sfb_bytes);
           tma_load_2d(a_dst, &tmap_w, &full[stage], 0, (wtile + kb) * kBM);
           bulk_load(smem + C::kOffSfa + stage * C::kKBS * 512, sfa_src + (size_t)kb * 512, nk * 512, &full[stage]);
-          bulk_load(smem + C::kOffSfb + stage * C::kKBS * 512, sfb_src + (size_t)kb * 512, sfb_bytes, &full[stage]);
+          bulk_load(smem + C::kOffSfb + stage * C::kKBS * C::kTokChunk, sfb_src + (size_t)kb * C::kTokChunk, sfb_bytes,
+                    &full[stage]);
           for (int i = 0; i < nk; ++i)
             tma_load_2d(b_dst + i * C::kBTile, &tmap_b, &full[stage], (kb + i) * kBK, ti.s0);
         }
@@ -333,11 +346,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
         tc_fence_after();
         if (lane == 0) {
           for (int i = 0; i < nk; ++i) {
-            const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + 8 * (stage * C::kKBS + i));
+            const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + C::kSfSlot * (stage * C::kKBS + i));
             const uint32_t sfa = smem_u32(smem + C::kOffSfa + (stage * C::kKBS + i) * 512);
-            const uint32_t sfb = smem_u32(smem + C::kOffSfb + (stage * C::kKBS + i) * 512);
+            const uint32_t sfb = smem_u32(smem + C::kOffSfb + (stage * C::kKBS + i) * C::kTokChunk);
             tc_cp_32x128b_warpx4(sf_col, make_smem_desc(sfa, 0, 128, kSwizzleNone));
-            tc_cp_32x128b_warpx4(sf_col + 4, make_smem_desc(sfb, 0, 128, kSwizzleNone));
+            // token scales: one 128-row group per 4 TMEM columns
+            for (int gq = 0; gq < C::kSfbGroups && gq * 128 < (int)n_mma; ++gq)
+              tc_cp_32x128b_warpx4(sf_col + 4 + 4 * gq, make_smem_desc(sfb + gq * 512, 0, 128, kSwizzleNone));
             const uint32_t a_base = smem_u32(smem + C::kOffA + stage * C::kABytes + i * C::kATile);
             const uint32_t b_base = smem_u32(smem + C::kOffB + stage * C::kBBytes + i * C::kBTile);
 #pragma unroll
@@ -365,28 +380,40 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
     mbar_wait(mma_done, 0, status, kWaitLimit, kWaitMmaDone, 0);
   } else {
     // ------------------------------------------------------------ epilogue
+    // kEpiWarps warps: quadrant q = warp % 4 of the TMEM lanes; with 8 warps the
+    // two halves take alternate 16-column chunks, each with its own staging
+    // buffer and named barrier.
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
-    const int et = threadIdx.x - 64;         // 0..127
-    float *ebuf_f = reinterpret_cast<float *>(smem + C::kOffEpi);
-    uint16_t *ebuf_h = reinterpret_cast<uint16_t *>(smem + C::kOffEpi);
+    const int eh = (warp - 2) >> 2;          // epilogue half
+    const int et = threadIdx.x - 64;         // 0 .. 32 * kEpiWarps - 1
+    const uint32_t bar_half = 2 + eh;
+    float *ebuf_f = reinterpret_cast<float *>(smem + C::kOffEpi + 4096 * eh);
+    uint16_t *ebuf_h = reinterpret_cast<uint16_t *>(smem + C::kOffEpi + 4096 * eh);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
       const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      // a half may start this item while the other still reads the previous
+      // item's row info, so it lives in the buffer of this item's accumulator
+      // (reused two items later, after every warp passed this item's vote)
+      int32_t *row_pair = row_pair_buf + acc * BN;
+      float *row_w = row_w_buf + acc * BN;
       if (et < ti.valid) {
         if (PHASE == 1) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
         else row_pair[et] = __ldg(args.perm + ti.s0 + et);
       }
-      // the four epilogue warps agree on the outcome of the bounded wait before
-      // any of them enters another named barrier
+      // the epilogue warps agree on the outcome of the bounded wait before any
+      // of them enters another named barrier
       const bool got = __all_sync(0xffffffffu,
                                   MXQ_TIMED_WAIT(3, mbar_wait(&tmem_full[acc], acc_phase, status, kWaitLimit, kWaitEpiTmemFull, w)));
-      if (lane == 0) vote[q] = got ? 1 : 0;
-      named_bar_sync(1, kEpiThreads);
-      if (!(vote[0] & vote[1] & vote[2] & vote[3])) break;
+      if (lane == 0) vote[warp - 2] = got ? 1 : 0;
+      named_bar_sync(1, 32 * C::kEpiWarps);
+      bool all_got = true;
+      for (int i = 0; i < C::kEpiWarps; ++i) all_got = all_got && vote[i] != 0;
+      if (!all_got) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
-      for (int c0 = 0; c0 < ti.valid; c0 += kChunk) {
+      for (int c0 = kChunk * eh; c0 < ti.valid; c0 += kChunk * C::kEpiHalves) {
         uint32_t v[16];
         tmem_ld_32x32b_x16(t_row + (uint32_t)c0, v);
         tmem_ld_wait();
@@ -407,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
               ebuf_f[j * 64 + feat] = h;
             }
           }
-          named_bar_sync(1, kEpiThreads);
+          named_bar_sync(bar_half, 128);
           // requantise: 16 columns x 2 groups of 32 features, 8 items per warp
 #pragma unroll 1
           for (int it = q; it < 2 * kChunk; it += 4) {
@@ -424,11 +451,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             if (lane == 0) {
               const int fg = fcol >> 5;                               // 32-group index along I
               const size_t chunk = (size_t)ti.g * (args.I / 128) + (fg >> 2);
-              args.sfb2[chunk * 512 + (c & 31) * 16 + (c >> 5) * 4 + (fg & 3)] = (uint8_t)(e + 127);
+              const int cr = c & 127;
+              args.sfb2[chunk * C::kTokChunk + (c >> 7) * 512 + (cr & 31) * 16 + (cr >> 5) * 4 + (fg & 3)] =
+                  (uint8_t)(e + 127);
               if (args.hs_out) args.hs_out[s * (args.I / 32) + fg] = (uint8_t)(e + 127);
             }
           }
-          named_bar_sync(1, kEpiThreads);
+          named_bar_sync(bar_half, 128);
         } else {
           const int row = 32 * q + lane;                             // output feature inside the tile
 #pragma unroll
@@ -436,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
             const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
             ebuf_h[j * 128 + row] = *reinterpret_cast<const uint16_t *>(&b);
           }
-          named_bar_sync(1, kEpiThreads);
+          named_bar_sync(bar_half, 128);
 #pragma unroll
           for (int it = 0; it < 2; ++it) {
             const int col = q + 4 * (2 * it + (lane >> 4));
@@ -449,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BN>::kCtasPerSm)
               *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(ebuf_h + col * 128 + l16 * 8);
             }
           }
-          named_bar_sync(1, kEpiThreads);
+          named_bar_sync(bar_half, 128);
         }
       }
       tc_fence_before();
@@ -496,6 +525,8 @@ __global__ void __launch_bounds__(256) prep_pool_kernel(const uint8_t *__restric
                                                         uint4 *__restrict__ xq_pool, int row16) {
   extern __shared__ int sh[];
   int *tile_off = sh, *cnt_sm = sh + (E + 1), *off_sm = sh + 2 * (E + 1);
+  pdl_launch_dependents();
+  pdl_wait();
   load_expert_table(counts, offsets, E, cnt_sm, off_sm);
   __syncthreads();
   if (threadIdx.x < 32) scan_tile_map<BN>(cnt_sm, E, tile_off);
@@ -528,9 +559,84 @@ __global__ void __launch_bounds__(256) prep_pool_kernel(const uint8_t *__restric
     const uint32_t *src = reinterpret_cast<const uint32_t *>(src_scales + (size_t)row * KB * 4);
     for (int kb = lane; kb < KB; kb += 32) {
       const uint32_t wv = __ldg(src + kb);
-      *reinterpret_cast<uint32_t *>(chunks + ((size_t)g * KB + kb) * 512 + (r & 31) * 16 + (r >> 5) * 4) = wv;
+      const int rr = r & 127;
+      *reinterpret_cast<uint32_t *>(chunks + ((size_t)g * KB + kb) * Cfg<BN>::kTokChunk + (r >> 7) * 512 +
+                                    (rr & 31) * 16 + (rr >> 5) * 4) = wv;
     }
   }
+}
+
+// The activation cast fused with the pool rows of GEMM1 (used by moe_forward):
+// for pool row s (expert e, tile g, row r) with pair p = perm[s] and token
+// t = p / k, write tok_pool[s] = t, w_pool[s] = topk_w[p], the E4M3 codes of
+// x[t] to xq_pool[s] and its UE8M0 scales straight into GEMM1's scale chunks.
+// One thread per 8 values of one pool row (four neighbouring lanes form a
+// 32-group), so every load of the step is in flight at once; a token routed
+// to k experts is cast k times, reading x[t] from L2, which saves writing and
+// re-reading a token-order copy.
+template <int BN>
+__global__ void __launch_bounds__(256) pool_cast_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ counts,
+                                                        const int32_t *__restrict__ offsets,
+                                                        const int32_t *__restrict__ perm,
+                                                        const float *__restrict__ topk_w, int E, int k, int H,
+                                                        uint8_t *__restrict__ chunks, int32_t *__restrict__ tok_pool,
+                                                        float *__restrict__ w_pool, uint2 *__restrict__ xq_pool) {
+  extern __shared__ int sh[];
+  int *tile_off = sh, *cnt_sm = sh + (E + 1), *off_sm = sh + 2 * (E + 1);
+  pdl_launch_dependents();
+  pdl_wait();
+  load_expert_table(counts, offsets, E, cnt_sm, off_sm);
+  __syncthreads();
+  if (threadIdx.x < 32) scan_tile_map<BN>(cnt_sm, E, tile_off);
+  __syncthreads();
+  const int P = off_sm[E];
+  const int H8 = H / 8, KB = H / 128;
+  const int64_t items = (int64_t)P * H8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < items; base += stride) {
+    const int64_t i = base + threadIdx.x;
+    const bool valid = i < items;               // groups of 4 items are all valid or all not
+    int s = 0, c = 0, t = 0, p = 0;
+    if (valid) {
+      s = (int)(i / H8);
+      c = (int)(i - (int64_t)s * H8);
+      p = __ldg(perm + s);
+      t = p / k;
+    }
+    uint8_t sb;
+    const uint2 codes = cast8_e4m3(valid ? __ldg(x + (size_t)t * H8 + c) : make_uint4(0, 0, 0, 0), valid, &sb);
+    if (!valid) continue;
+    xq_pool[(size_t)s * H8 + c] = codes;
+    if ((c & 3) == 0) {
+      int lo = 0, hi = E;                      // expert e with off[e] <= s < off[e+1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off_sm[mid] <= s) lo = mid; else hi = mid;
+      }
+      const int rank = s - off_sm[lo];
+      const int g = tile_off[lo] + rank / BN, r = rank % BN;
+      const int rr = r & 127;
+      chunks[((size_t)g * KB + (c >> 4)) * Cfg<BN>::kTokChunk + (r >> 7) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 +
+             ((c >> 2) & 3)] = sb;
+      if (c == 0) {
+        tok_pool[s] = t;
+        w_pool[s] = __ldg(topk_w + p);
+      }
+    }
+  }
+}
+
+template <int BN>
+int launch_pool_cast_t(const moe_expert_args *a, const uint16_t *x, char *ws, const ExpertWs &lay, cudaStream_t st) {
+  const int64_t P = a->T * a->k;
+  const size_t sm = (size_t)3 * (a->E + 1) * 4;
+  const int64_t blocks = ceil_div(P * (a->H / 8), 256);
+  const int cap = num_sms() * 8;
+  const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+  return launch_pdl(pool_cast_kernel<BN>, dim3(grid), dim3(256), sm, st, reinterpret_cast<const uint4 *>(x),
+                    a->counts, a->offsets, a->perm, a->topk_w, a->E, a->k, (int)a->H,
+                    reinterpret_cast<uint8_t *>(ws + lay.sfb1), reinterpret_cast<int32_t *>(ws + lay.tok_pool),
+                    reinterpret_cast<float *>(ws + lay.w_pool), reinterpret_cast<uint2 *>(ws + lay.xq_pool));
 }
 
 template <int BN, bool FROM_TOKENS>
@@ -541,10 +647,9 @@ int launch_prep(const uint8_t *src, const moe_expert_args *a, int KB, uint8_t *c
   const int64_t blocks = ceil_div(P, 8);
   const int cap = num_sms() * 4;
   const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
-  prep_pool_kernel<BN, FROM_TOKENS><<<grid, 256, sm, st>>>(
-      src, a->counts, a->offsets, a->perm, a->topk_w, a->E, a->k, KB, chunks, tok_pool, w_pool,
-      reinterpret_cast<const uint4 *>(a->xq), reinterpret_cast<uint4 *>(xq_pool), (int)(a->H / 16));
-  return launch_status();
+  return launch_pdl(prep_pool_kernel<BN, FROM_TOKENS>, dim3(grid), dim3(256), sm, st, src, a->counts, a->offsets,
+                    a->perm, a->topk_w, a->E, a->k, KB, chunks, tok_pool, w_pool,
+                    reinterpret_cast<const uint4 *>(a->xq), reinterpret_cast<uint4 *>(xq_pool), (int)(a->H / 16));
 }
 
 template <int BN>
@@ -602,8 +707,8 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
-    expert_gemm_kernel<BN, 1><<<grid, kThreads, sm, st>>>(tw1, tb, g);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_pdl(expert_gemm_kernel<BN, 1>, dim3(grid), dim3(C::kThreads), sm, st, tw1, tb, g) != MOE_OK)
+      return MOE_ERR_CUDA;
   }
   if (phases & MOE_PHASE_GEMM2) {
     // GEMM2 -> BF16 per pair
@@ -621,13 +726,28 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
-    expert_gemm_kernel<BN, 2><<<grid, kThreads, sm, st>>>(tw2, th, g);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(grid), dim3(C::kThreads), sm, st, tw2, th, g) != MOE_OK)
+      return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }
 
 }  // namespace
+
+int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch, cudaStream_t st) {
+  const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
+  if (a->T == 0) return MOE_OK;
+  char *ws = reinterpret_cast<char *>(scratch);
+  const int bn = a->tile_n ? a->tile_n : choose_tile_n(a->T * a->k, a->E);
+  switch (bn) {
+    case 16: return launch_pool_cast_t<16>(a, x, ws, lay, st);
+    case 32: return launch_pool_cast_t<32>(a, x, ws, lay, st);
+    case 64: return launch_pool_cast_t<64>(a, x, ws, lay, st);
+    case 128: return launch_pool_cast_t<128>(a, x, ws, lay, st);
+    case 224: return launch_pool_cast_t<224>(a, x, ws, lay, st);
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
 
 int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, cudaStream_t st) {
   const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
@@ -639,6 +759,7 @@ int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, 
     case 32: return run_expert<32>(a, status, ws, lay, st);
     case 64: return run_expert<64>(a, status, ws, lay, st);
     case 128: return run_expert<128>(a, status, ws, lay, st);
+    case 224: return run_expert<224>(a, status, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
 }
@@ -651,7 +772,8 @@ int check_expert_args(const moe_expert_args *a, bool need_ws) {
   if (a->T * (int64_t)a->k >= ((int64_t)1 << 31) || a->H * a->E >= ((int64_t)1 << 31) ||
       2 * a->I * a->E >= ((int64_t)1 << 31))
     return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (a->tile_n != 0 && a->tile_n != 16 && a->tile_n != 32 && a->tile_n != 64 && a->tile_n != 128)
+  if (a->tile_n != 0 && a->tile_n != 16 && a->tile_n != 32 && a->tile_n != 64 && a->tile_n != 128 &&
+      a->tile_n != 224)
     return MOE_ERR_INVALID_ARG;
   if (a->phases & ~15) return MOE_ERR_INVALID_ARG;
   if ((a->phases & MOE_PHASE_H_SCALES) && (!a->hq || !a->hs)) return MOE_ERR_INVALID_ARG;

@@ -6,7 +6,9 @@
 #include <cuda_runtime.h>
 
 #include <cstddef>
+#include <algorithm>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/moe_mxq.h"
 
@@ -20,6 +22,25 @@ inline int launch_status() {
 }
 
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Launches a kernel with programmatic stream serialization, so that it may
+// start while the previous kernel of the stream finishes (each kernel waits
+// with griddepcontrol.wait before touching global memory).  Returns a status.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Number of SMs of the current device (cached per device).
@@ -49,11 +70,13 @@ inline int64_t max_token_tiles(int64_t P, int64_t E, int64_t bn) {
 
 inline ExpertWs expert_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   const int64_t P = T * k;
-  const int64_t tiles = max_token_tiles(P, E, 16);   // smallest tile -> most tiles
+  // token-scale chunks: the most (tiles x chunk bytes) over the tile sizes
+  // (16 tokens: most tiles, 512 B chunks; 224 tokens: 1 KB chunks)
+  const int64_t chunks = std::max(max_token_tiles(P, E, 16) * 512, max_token_tiles(P, E, 224) * 1024);
   ExpertWs w;
   size_t off = 0;
-  w.sfb1 = off;    off += round_up((size_t)tiles * (size_t)(H / 128) * 512, 256);
-  w.sfb2 = off;    off += round_up((size_t)tiles * (size_t)(I / 128) * 512, 256);
+  w.sfb1 = off;    off += round_up((size_t)chunks * (size_t)(H / 128), 256);
+  w.sfb2 = off;    off += round_up((size_t)chunks * (size_t)(I / 128), 256);
   w.hq = off;      off += round_up((size_t)P * (size_t)I, 256);
   w.tok_pool = off; off += round_up((size_t)P * 4, 256);
   w.w_pool = off;  off += round_up((size_t)P * 4, 256);
@@ -65,15 +88,17 @@ inline ExpertWs expert_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int
 // Every public workspace starts with this many bytes of status words.
 constexpr size_t kStatusBytes = 256;
 
-// Token tile chosen from the mean number of pairs per routed expert (tiles up
-// to 64 run two CTAs per SM; 128 only pays off for heavily loaded experts).
+// Token tile chosen from the mean number of pairs per routed expert: tiles up
+// to 64 tokens run two CTAs per SM; above that a 224-token tile gives each
+// tcgen05 instruction more tensor work (the MMA's N follows the tile's valid
+// tokens rounded up to 16).
 inline int choose_tile_n(int64_t P, int64_t E) {
   const int64_t ne = E < P ? E : P;
   const int64_t mean = ne > 0 ? ceil_div(P, ne) : 1;
   if (mean <= 16) return 16;
   if (mean <= 32) return 32;
-  if (mean <= 192) return 64;
-  return 128;
+  if (mean <= 64) return 64;
+  return 224;
 }
 
 // Internal launchers (return a moe_status).  `status` points at the two
@@ -85,6 +110,9 @@ int launch_permute(const int32_t *idx, int64_t T, int E, int k, int32_t *counts,
                    int32_t *perm, int32_t *inv_perm, int *status, void *scratch, cudaStream_t st);
 int check_expert_args(const moe_expert_args *a, bool need_ws);
 int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, cudaStream_t st);
+// Activation cast straight into GEMM1's pool rows and scale chunks (replaces
+// mxq_quantize_act + the token-scale step inside moe_forward).
+int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch, cudaStream_t st);
 int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k, int64_t H, uint16_t *y,
                    cudaStream_t st);
 

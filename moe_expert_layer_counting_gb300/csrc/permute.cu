@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kThreads) perm_count_kernel(const int32_t *__r
                                                               int E, int64_t chunk, int32_t *__restrict__ hist,
                                                               int *ws_status) {
   extern __shared__ int cnt[];
+  pdl_launch_dependents();
+  pdl_wait();
   for (int e = threadIdx.x; e < E; e += kThreads) cnt[e] = 0;
   __syncthreads();
   const int64_t lo = (int64_t)blockIdx.x * chunk;
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(kThreads) perm_scatter_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t lo = (int64_t)blockIdx.x * chunk;
   const int64_t hi = lo + chunk < P ? lo + chunk : P;
+  pdl_launch_dependents();
+  pdl_wait();
 
   // 1. totals and this block's base inside every bucket
   int tot = 0, pre = 0;
@@ -195,12 +199,12 @@ int launch_permute(const int32_t *idx, int64_t T, int E, int k, int32_t *counts,
           cudaSuccess)
     return MOE_ERR_CUDA;
   if (pl.nb > 1) {
-    perm_count_kernel<<<pl.nb, kThreads, (size_t)E * 4, st>>>(idx, pl.P, E, pl.chunk, hist, status);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_pdl(perm_count_kernel, dim3(pl.nb), dim3(kThreads), (size_t)E * 4, st, idx, pl.P, E, pl.chunk, hist,
+                   status) != MOE_OK)
+      return MOE_ERR_CUDA;
   }
-  perm_scatter_kernel<<<pl.nb, kThreads, sm, st>>>(idx, pl.P, E, pl.chunk, pl.nb, hist, counts, offsets, perm,
-                                                   inv_perm, status);
-  return launch_status();
+  return launch_pdl(perm_scatter_kernel, dim3(pl.nb), dim3(kThreads), sm, st, idx, pl.P, E, pl.chunk, pl.nb,
+                    (const int32_t *)hist, counts, offsets, perm, inv_perm, status);
 }
 
 }  // namespace mxq

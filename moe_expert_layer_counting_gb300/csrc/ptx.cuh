@@ -31,6 +31,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel of the stream is still running.  pdl_wait() blocks until
+// that kernel has completed and its memory is visible; every kernel here
+// calls it before its first global-memory access, so only setup that touches
+// no global memory (barrier init, TMEM allocation, tensor-map prefetch)
+// overlaps the previous kernel.  pdl_launch_dependents() lets the next kernel
+// of the stream be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -260,5 +271,33 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// One lane's share of the activation cast: 8 consecutive BF16 values (one
+// 16-byte load), four neighbouring lanes forming one 32-group.  All 32 lanes
+// of the warp must call it together (`valid` false for lanes without data).
+// Returns the 8 E4M3 codes; *scale_byte gets the group's UE8M0 byte.
+__device__ __forceinline__ uint2 cast8_e4m3(const uint4 &v, bool valid, uint8_t *scale_byte) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+    f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+  }
+  if (valid) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int e = ue8m0_exponent<true>(amax);
+  const float inv = pow2_neg(e);
+  uint32_t c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) c[j] = cvt_e4m3x2(f[2 * j] * inv, f[2 * j + 1] * inv);
+  *scale_byte = (uint8_t)(e + 127);
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
 
 }  // namespace mxq

@@ -35,26 +35,17 @@ __device__ __forceinline__ float group4_amax(float a) {
 // [rows][K] array, so the 32-group of item i is i / 4.
 __global__ void __launch_bounds__(kThreads) quant_act_kernel(const uint4 *__restrict__ x, int64_t items,
                                                              uint2 *__restrict__ q, uint8_t *__restrict__ s) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < items; base += stride) {
     const int64_t i = base + threadIdx.x;
     const bool valid = i < items;
-    float f[8];
-    float amax = 0.f;
-    if (valid) {
-      unpack8(__ldg(x + i), f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    }
-    amax = group4_amax(amax);
+    uint8_t sb;
+    const uint2 codes = cast8_e4m3(valid ? __ldg(x + i) : make_uint4(0, 0, 0, 0), valid, &sb);
     if (!valid) continue;
-    const int e = ue8m0_exponent<true>(amax);
-    const float inv = pow2_neg(e);
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = cvt_e4m3x2(f[2 * j] * inv, f[2 * j + 1] * inv);
-    q[i] = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-    if ((i & 3) == 0) s[i >> 2] = (uint8_t)(e + 127);
+    q[i] = codes;
+    if ((i & 3) == 0) s[i >> 2] = sb;
   }
 }
 
@@ -68,6 +59,8 @@ __global__ void __launch_bounds__(kThreads) quant_weight_kernel(const uint4 *__r
                                                                 int64_t N, int64_t K, int layout,
                                                                 uint32_t *__restrict__ q,
                                                                 uint8_t *__restrict__ s) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t items = G * N * K / 8;
   const int64_t items_per_row = K / 8;
   const int64_t half = N / 2;
@@ -132,9 +125,8 @@ int grid_for(int64_t items) {
 int launch_quant_act(const uint16_t *x, int64_t rows, int64_t K, uint8_t *q, uint8_t *s, cudaStream_t st) {
   const int64_t items = rows * K / 8;
   if (items == 0) return MOE_OK;
-  quant_act_kernel<<<grid_for(items), kThreads, 0, st>>>(reinterpret_cast<const uint4 *>(x), items,
-                                                         reinterpret_cast<uint2 *>(q), s);
-  return launch_status();
+  return launch_pdl(quant_act_kernel, dim3(grid_for(items)), dim3(kThreads), 0, st,
+                    reinterpret_cast<const uint4 *>(x), items, reinterpret_cast<uint2 *>(q), s);
 }
 
 }  // namespace mxq
@@ -163,7 +155,6 @@ extern "C" int mxq_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int6
   if (!w || !q || !s) return MOE_ERR_INVALID_ARG;
   if (!aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_MISALIGNED;
   const int64_t items = G * N * K / 8;
-  quant_weight_kernel<<<grid_for(items), kThreads, 0, stream>>>(reinterpret_cast<const uint4 *>(w), G, N, K,
-                                                                layout, reinterpret_cast<uint32_t *>(q), s);
-  return launch_status();
+  return launch_pdl(quant_weight_kernel, dim3(grid_for(items)), dim3(kThreads), 0, stream,
+                    reinterpret_cast<const uint4 *>(w), G, N, K, layout, reinterpret_cast<uint32_t *>(q), s);
 }

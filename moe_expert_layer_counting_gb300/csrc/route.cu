@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
                                                             int k, int32_t *__restrict__ idx,
                                                             float *__restrict__ w) {
   extern __shared__ float sm[];                       // kWarps x E logits
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float *row = sm + (size_t)warp * E;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < T; t += (int64_t)gridDim.x * kWarps) {
@@ -76,8 +78,7 @@ int launch_route(const float *logits, int64_t T, int E, int k, int32_t *idx, flo
         cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  route_kernel<<<grid, kWarps * 32, smem, st>>>(logits, T, E, k, idx, w);
-  return launch_status();
+  return launch_pdl(route_kernel, dim3(grid), dim3(kWarps * 32), smem, st, logits, T, E, k, idx, w);
 }
 
 }  // namespace mxq

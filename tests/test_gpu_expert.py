@@ -116,7 +116,7 @@ def _compare_pairs(st, y_pairs_g, hq_g, hs_g, y_ref, hq_ref, hs_ref, what):
     Hp.assert_bf16_close(y_pairs_g[j, t], y_ref[j, t], what=what)
 
 
-@pytest.mark.parametrize("tile_n", [16, 32, 64, 128])
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 224])
 def test_expert_forward_tiny_every_tile(B, tile_n):
     st = Setup(B, W.WORKLOADS["tiny"])
     st.check_weights_bitexact()
@@ -202,7 +202,7 @@ def test_large_workloads_sampled(B, wl_name):
     assert np.array_equal(y_fwd, want)
 
 
-@pytest.mark.parametrize("wl_name,tile_n", [("tiny", 16), ("tiny", 128), ("small_decode", 0)])
+@pytest.mark.parametrize("wl_name,tile_n", [("tiny", 16), ("tiny", 128), ("tiny", 224), ("small_decode", 0)])
 def test_gemm2_on_oracle_h(B, wl_name, tile_n):
     """GEMM2 alone, fed with the oracle's own requantised h (pool order): the
     only difference left is FP32 accumulation before the BF16 cast, so the
