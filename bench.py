@@ -163,7 +163,7 @@ def run_ours(args, rank, world, local_rank):
     from moe_expert_layer_counting_gb300 import binding as B
     from moe_expert_layer_counting_gb300.layer import QuantizedExperts
 
-    wl = W.WORKLOADS[args.workload]
+    wl = W.WORKLOADS.get(args.workload) or W.PROFILE_WORKLOADS[args.workload]
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)

@@ -61,9 +61,9 @@ constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in H
 // streams without changing any accumulation order.
 template <int BN>
 struct Cfg {
-  // tiles above 128 tokens: one K block per stage, scales of the token operand
-  // in two 128-row groups, and an 8-warp epilogue (two warps per TMEM quadrant)
-  static constexpr int kKBS = (BN == 64 || BN > 128) ? 1 : 2;
+  // tiles above 128 tokens: scales of the token operand in two 128-row
+  // groups, and an 8-warp epilogue (two warps per TMEM quadrant)
+  static constexpr int kKBS = BN == 64 ? 1 : 2;
   static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
   static constexpr int kSfbGroups = (BN + 127) / 128;       // 128-row groups of token scales
   static constexpr int kTokChunk = 512 * kSfbGroups;        // bytes of one (tile, K block) token-scale chunk

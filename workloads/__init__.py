@@ -53,6 +53,12 @@ WORKLOADS = {
                                seed=4, zipf_s=1.2),
 }
 
+# Smaller cases with the same per-expert shapes, for profiler captures that
+# must stay small (the prefill's ~128 pairs per expert on 32 experts).
+PROFILE_WORKLOADS = {
+    "prefill_e32": Workload("prefill_e32", T=512, H=7168, I=2048, E=32, k=8, sigma=0.01, seed=3),
+}
+
 
 def bf16_bits(t: torch.Tensor) -> torch.Tensor:
     """Bit patterns (int16 view) of a BF16 tensor."""
