@@ -144,13 +144,22 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
+  const int64_t P = a->T * a->k;
+  ea.tile_n = a->tile_n ? a->tile_n : choose_tile_n(P, a->E);
+  int32_t *inv_perm = reinterpret_cast<int32_t *>(ws + lay.inv_perm);
+  if (front_eligible(a->T, a->H, a->E, a->k)) {
+    // small problems: routing + permute + pool cast in one launch
+    rc = launch_front(&ea, a->x, a->logits, idx, wts, inv_perm, ws + lay.expert, st);
+    if (rc != MOE_OK) return rc;
+    ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
+    rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
+    if (rc != MOE_OK) return rc;
+    return launch_combine(ea.y_pairs, idx, a->T, a->k, a->H, a->y, st);
+  }
   rc = launch_route(a->logits, a->T, a->E, a->k, idx, wts, st);
   if (rc != MOE_OK) return rc;
-  const int64_t P = a->T * a->k;
-  rc = launch_permute(idx, a->T, a->E, a->k, counts, offsets, perm, reinterpret_cast<int32_t *>(ws + lay.inv_perm),
-                      status, ws + lay.perm_scratch, st);
+  rc = launch_permute(idx, a->T, a->E, a->k, counts, offsets, perm, inv_perm, status, ws + lay.perm_scratch, st);
   if (rc != MOE_OK) return rc;
-  ea.tile_n = a->tile_n ? a->tile_n : choose_tile_n(P, a->E);
   if (P * a->H <= kPoolCastMaxValues) {
     // small problems: cast x straight into GEMM1's pool rows and scale chunks
     // (one launch, every load in flight at once)

@@ -37,6 +37,7 @@
 #include <cstdlib>
 
 #include "host_common.h"
+#include "layer_blocks.cuh"
 #include "ptx.cuh"
 
 namespace mxq {
@@ -626,6 +627,138 @@ __global__ void __launch_bounds__(256) pool_cast_kernel(const uint4 *__restrict_
   }
 }
 
+// Small problems in one launch.  Every CTA routes all T tokens and builds the
+// whole counting-sort permutation in shared memory -- the same result in every
+// CTA, so no grid-wide synchronisation is needed -- CTA 0 writes the routing
+// and permute outputs, and every CTA then casts its share of the pool rows
+// exactly as pool_cast_kernel does.  Used for T <= 64, E <= 256 (a few KB of
+// logits per CTA).
+constexpr int kFrontThreads = 256;
+constexpr int kFrontMaxT = 64, kFrontMaxE = 256;
+
+template <int BN>
+__global__ void __launch_bounds__(kFrontThreads) front_kernel(
+    const float *__restrict__ logits, const uint4 *__restrict__ x, int T, int E, int k, int H,
+    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts_out,
+    int32_t *__restrict__ offsets_out, int32_t *__restrict__ perm_out, int32_t *__restrict__ inv_perm_out,
+    uint8_t *__restrict__ chunks, int32_t *__restrict__ tok_pool, float *__restrict__ w_pool,
+    uint2 *__restrict__ xq_pool) {
+  constexpr int kW = kFrontThreads / 32;
+  extern __shared__ __align__(16) unsigned char fsm[];
+  const int P = T * k;
+  float *rows = reinterpret_cast<float *>(fsm);                        // [kW][E]
+  int *idx_sm = reinterpret_cast<int *>(rows + kW * E);                // [P]
+  float *w_sm = reinterpret_cast<float *>(idx_sm + P);                 // [P]
+  int *perm_sm = reinterpret_cast<int *>(w_sm + P);                    // [P]
+  int *cnt = perm_sm + P;                                              // [E+1]
+  int *off = cnt + (E + 1);                                            // [E+1]
+  int *tile_off = off + (E + 1);                                       // [E+1]
+  int *base = tile_off + (E + 1);                                      // [E]
+  int *warp_sums = base + E;                                           // [kW]
+  int *total = warp_sums + kW;                                         // [1]
+  uint16_t *wc = reinterpret_cast<uint16_t *>(total + 4);              // [kW][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool writer = blockIdx.x == 0;
+  pdl_launch_dependents();
+  pdl_wait();
+  // 1. routing of every token, one warp per token
+  for (int t = warp; t < T; t += kW) {
+    float *row = rows + warp * E;
+    for (int e = lane; e < E; e += 32) row[e] = __ldg(logits + (size_t)t * E + e);
+    __syncwarp();
+    int my_idx;
+    float my_w;
+    warp_route_token(row, E, k, lane, &my_idx, &my_w);
+    if (lane < k) {
+      idx_sm[t * k + lane] = my_idx;
+      w_sm[t * k + lane] = my_w;
+      if (writer) {
+        idx_out[t * k + lane] = my_idx;
+        w_out[t * k + lane] = my_w;
+      }
+    }
+    __syncwarp();
+  }
+  for (int e = tid; e <= E; e += kFrontThreads) cnt[e] = 0;
+  __syncthreads();
+  // 2. count -> prefix -> stable scatter
+  for (int p = tid; p < P; p += kFrontThreads) atomicAdd(&cnt[idx_sm[p]], 1);
+  __syncthreads();
+  const int o = block_exclusive_scan<kFrontThreads>(tid < E ? cnt[tid] : 0, warp_sums, total);
+  if (tid < E) {
+    off[tid] = o;
+    base[tid] = o;
+    if (writer) {
+      counts_out[tid] = cnt[tid];
+      offsets_out[tid] = o;
+    }
+  }
+  if (tid == 0) {
+    off[E] = *total;
+    if (writer) offsets_out[E] = *total;
+  }
+  __syncthreads();
+  if (warp == 0) scan_tile_map<BN>(cnt, E, tile_off);
+  block_stable_ranks<kFrontThreads>([&](int64_t p) { return idx_sm[p]; }, 0, P, E, base, wc,
+                                    writer ? perm_out : nullptr, writer ? inv_perm_out : nullptr, perm_sm);
+  // 3. this CTA's share of the pool rows
+  const int H8 = H / 8, KB = H / 128;
+  const int64_t items = (int64_t)P * H8;
+  const int64_t stride = (int64_t)gridDim.x * kFrontThreads;
+  for (int64_t b0 = (int64_t)blockIdx.x * kFrontThreads; b0 < items; b0 += stride) {
+    const int64_t i = b0 + tid;
+    const bool valid = i < items;
+    int sr = 0, c = 0, t = 0, pp = 0;
+    if (valid) {
+      sr = (int)(i / H8);
+      c = (int)(i - (int64_t)sr * H8);
+      pp = perm_sm[sr];
+      t = pp / k;
+    }
+    uint8_t sb;
+    const uint2 codes = cast8_e4m3(valid ? __ldg(x + (size_t)t * H8 + c) : make_uint4(0, 0, 0, 0), valid, &sb);
+    if (!valid) continue;
+    xq_pool[(size_t)sr * H8 + c] = codes;
+    if ((c & 3) == 0) {
+      int lo = 0, hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= sr) lo = mid; else hi = mid;
+      }
+      const int rank = sr - off[lo];
+      const int g = tile_off[lo] + rank / BN, r = rank % BN;
+      const int rr = r & 127;
+      chunks[((size_t)g * KB + (c >> 4)) * Cfg<BN>::kTokChunk + (r >> 7) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 +
+             ((c >> 2) & 3)] = sb;
+      if (c == 0) {
+        tok_pool[sr] = t;
+        w_pool[sr] = w_sm[pp];
+      }
+    }
+  }
+}
+
+size_t front_smem(int T, int E, int k) {
+  const int P = T * k;
+  return (size_t)(kFrontThreads / 32) * E * 4 + (size_t)3 * P * 4 + (size_t)3 * (E + 1) * 4 + (size_t)E * 4 +
+         (kFrontThreads / 32) * 4 + 16 + (size_t)(kFrontThreads / 32) * E * 2;
+}
+
+template <int BN>
+int launch_front_t(const moe_expert_args *a, const uint16_t *x, const float *logits, int32_t *idx, float *wts,
+                   int32_t *inv_perm, char *ws, const ExpertWs &lay, cudaStream_t st) {
+  const int64_t P = a->T * a->k;
+  const int64_t blocks = ceil_div(P * (a->H / 8), kFrontThreads);
+  const int cap = num_sms() * 2;
+  const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+  return launch_pdl(front_kernel<BN>, dim3(grid), dim3(kFrontThreads), front_smem((int)a->T, a->E, a->k), st, logits,
+                    reinterpret_cast<const uint4 *>(x), (int)a->T, a->E, a->k, (int)a->H, idx, wts,
+                    const_cast<int32_t *>(a->counts), const_cast<int32_t *>(a->offsets),
+                    const_cast<int32_t *>(a->perm), inv_perm, reinterpret_cast<uint8_t *>(ws + lay.sfb1),
+                    reinterpret_cast<int32_t *>(ws + lay.tok_pool), reinterpret_cast<float *>(ws + lay.w_pool),
+                    reinterpret_cast<uint2 *>(ws + lay.xq_pool));
+}
+
 template <int BN>
 int launch_pool_cast_t(const moe_expert_args *a, const uint16_t *x, char *ws, const ExpertWs &lay, cudaStream_t st) {
   const int64_t P = a->T * a->k;
@@ -745,6 +878,25 @@ int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch,
     case 64: return launch_pool_cast_t<64>(a, x, ws, lay, st);
     case 128: return launch_pool_cast_t<128>(a, x, ws, lay, st);
     case 224: return launch_pool_cast_t<224>(a, x, ws, lay, st);
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
+bool front_eligible(int64_t T, int64_t H, int E, int k) {
+  return T >= 1 && T <= kFrontMaxT && E <= kFrontMaxE && T * k * H <= (int64_t(4) << 20);
+}
+
+int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int32_t *idx, float *wts,
+                 int32_t *inv_perm, void *scratch, cudaStream_t st) {
+  const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
+  char *ws = reinterpret_cast<char *>(scratch);
+  const int bn = a->tile_n ? a->tile_n : choose_tile_n(a->T * a->k, a->E);
+  switch (bn) {
+    case 16: return launch_front_t<16>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
+    case 32: return launch_front_t<32>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
+    case 64: return launch_front_t<64>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
+    case 128: return launch_front_t<128>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
+    case 224: return launch_front_t<224>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
 }

@@ -113,6 +113,12 @@ int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, 
 // Activation cast straight into GEMM1's pool rows and scale chunks (replaces
 // mxq_quantize_act + the token-scale step inside moe_forward).
 int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch, cudaStream_t st);
+// Small problems (front_eligible): routing, counting-sort permute and the pool
+// cast in one launch.  `a` supplies shapes, tile size and the counts / offsets /
+// perm outputs.
+bool front_eligible(int64_t T, int64_t H, int E, int k);
+int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int32_t *idx, float *wts,
+                 int32_t *inv_perm, void *scratch, cudaStream_t st);
 int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k, int64_t H, uint16_t *y,
                    cudaStream_t st);
 

@@ -17,6 +17,7 @@
 //                    warp match_any + a per-warp count table in shared memory.
 // With a single block the scatter kernel counts for itself (one launch).
 #include "host_common.h"
+#include "layer_blocks.cuh"
 #include "ptx.cuh"
 
 namespace mxq {
@@ -60,33 +61,6 @@ __global__ void __launch_bounds__(kThreads) perm_count_kernel(const int32_t *__r
   for (int e = threadIdx.x; e < E; e += kThreads) hist[(int64_t)blockIdx.x * E + e] = cnt[e];
 }
 
-// Exclusive scan of one value per thread over the block; returns the prefix
-// and writes the block total to *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) warp_sums[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int s = warp_sums[lane];
-    int si = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, si, o);
-      if (lane >= o) si += n;
-    }
-    warp_sums[lane] = si - s;                   // exclusive prefix of warp sums
-    if (lane == 31) *total = si;
-  }
-  __syncthreads();
-  return inc - v + warp_sums[warp];
-}
-
 __global__ void __launch_bounds__(kThreads) perm_scatter_kernel(
     const int32_t *__restrict__ idx, int64_t P, int E, int64_t chunk, int nb,
     const int32_t *__restrict__ hist, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
@@ -98,7 +72,7 @@ __global__ void __launch_bounds__(kThreads) perm_scatter_kernel(
   int *total_sh = warp_sums + 32;                                   // [1]
   uint16_t *wc = reinterpret_cast<uint16_t *>(total_sh + 4);        // [32][E]
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int64_t lo = (int64_t)blockIdx.x * chunk;
   const int64_t hi = lo + chunk < P ? lo + chunk : P;
   pdl_launch_dependents();
@@ -124,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) perm_scatter_kernel(
     }
   }
   // 2. offsets = exclusive scan of the totals
-  const int off = block_exclusive_scan(tid < E ? tot : 0, warp_sums, total_sh);
+  const int off = block_exclusive_scan<kThreads>(tid < E ? tot : 0, warp_sums, total_sh);
   if (tid < E) base[tid] = off + pre;
   if (blockIdx.x == 0) {
     if (tid < E) {
@@ -136,43 +110,7 @@ __global__ void __launch_bounds__(kThreads) perm_scatter_kernel(
   __syncthreads();
 
   // 3. stable ranks, 1024 pairs at a time
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int64_t start = lo; start < hi; start += kThreads) {
-    uint32_t *wc32 = reinterpret_cast<uint32_t *>(wc);
-    for (int i = tid; i < 16 * E; i += kThreads) wc32[i] = 0u;
-    const int64_t p = start + tid;
-    int e = -1;
-    if (p < hi) {
-      e = __ldg(idx + p);
-      if (e >= E) e = -1;                       // reported by the count pass
-    }
-    __syncthreads();
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    const int lrank = __popc(peers & lt_mask);
-    if (e >= 0 && lrank == 0) wc[warp * E + e] = (uint16_t)__popc(peers);
-    __syncthreads();
-    int run = 0;
-    if (tid < E) {
-      for (int w = 0; w < 32; ++w) {
-        const int c = wc[w * E + tid];
-        wc[w * E + tid] = (uint16_t)run;
-        run += c;
-      }
-    }
-    __syncthreads();
-    if (p < hi) {
-      if (e >= 0) {
-        const int pos = base[e] + wc[warp * E + e] + lrank;
-        perm[pos] = (int32_t)p;
-        inv_perm[p] = pos;
-      } else {
-        inv_perm[p] = -1;
-      }
-    }
-    __syncthreads();
-    if (tid < E) base[tid] += run;
-    __syncthreads();
-  }
+  block_stable_ranks<kThreads>([&](int64_t p) { return (int)__ldg(idx + p); }, lo, hi, E, base, wc, perm, inv_perm);
 }
 
 size_t scatter_smem(int E) { return (size_t)(2 * kMaxE + 32 + 4) * 4 + (size_t)32 * E * 2; }

@@ -8,6 +8,7 @@
 // exp(l_j - l_max) / sum over the chosen k -- the full softmax denominator
 // cancels in the renormalisation.
 #include "host_common.h"
+#include "layer_blocks.cuh"
 #include "ptx.cuh"
 
 namespace mxq {
@@ -16,10 +17,6 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kMaxE = 1024;
-
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
 
 __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restrict__ logits, int64_t T, int E,
                                                             int k, int32_t *__restrict__ idx,
@@ -33,33 +30,12 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
     const float *src = logits + t * E;
     for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
     __syncwarp();
-    float my_val = 0.f;   // lane j < k keeps the j-th selection
-    int my_idx = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int e = lane; e < E; e += 32) {
-        const float v = row[e];
-        if (better(v, e, bv, bi)) { bv = v; bi = e; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if (lane == j) { my_val = bv; my_idx = bi; }
-      if (lane == (bi & 31)) row[bi] = -INFINITY;     // taken (logits are finite)
-      __syncwarp();
-    }
-    const float lmax = __shfl_sync(0xffffffffu, my_val, 0);
-    const float ex = lane < k ? expf(my_val - lmax) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    int my_idx;
+    float my_w;
+    warp_route_token(row, E, k, lane, &my_idx, &my_w);
     if (lane < k) {
       idx[t * k + lane] = my_idx;
-      w[t * k + lane] = __fdiv_rn(ex, sum);
+      w[t * k + lane] = my_w;
     }
     __syncwarp();
   }
