@@ -54,18 +54,19 @@ constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in H
 // Issue cost.  Every asynchronous instruction (TMA copy, tcgen05.cp,
 // tcgen05.mma) takes ~80 cycles of its issuing thread, whatever its size,
 // while one M=128 x N x K=32 MMA keeps the tensor core busy ~0.53 N cycles.
-// So (a) a pipeline stage of a decode-sized tile covers kKBS = 2 K blocks:
-// one TMA box of 256 weight rows (two consecutive tiles of the
-// tile-contiguous layout), one bulk copy per scale operand and one 2-D box of
-// token rows per K block; and (b) tiles up to N = 64 run two CTAs per SM
-// (half the shared memory each), giving the SM two independent MMA issue
-// streams without changing any accumulation order.
+// So (a) a pipeline stage may cover kKBS = 2 K blocks: one TMA box of 256
+// weight rows (two consecutive tiles of the tile-contiguous layout), one bulk
+// copy per scale operand and one 2-D box of token rows per K block; and (b)
+// small token tiles run several CTAs per SM (three for N = 16, two for
+// N <= 64, with one K block per stage where shared memory is tight), giving
+// the SM independent MMA issue streams without changing any accumulation
+// order.
 template <int BN>
 struct Cfg {
   // tiles above 128 tokens: scales of the token operand in two 128-row
   // groups, and an 8-warp epilogue (two warps per TMEM quadrant)
-  static constexpr int kKBS = BN == 64 ? 1 : 2;
-  static constexpr int kCtasPerSm = BN <= 64 ? 2 : 1;
+  static constexpr int kKBS = (BN == 16 || BN == 64) ? 1 : 2;
+  static constexpr int kCtasPerSm = BN == 16 ? 3 : (BN <= 64 ? 2 : 1);
   static constexpr int kSfbGroups = (BN + 127) / 128;       // 128-row groups of token scales
   static constexpr int kTokChunk = 512 * kSfbGroups;        // bytes of one (tile, K block) token-scale chunk
   static constexpr int kSfSlot = 4 + 4 * kSfbGroups;        // TMEM columns of one K block's scales
@@ -78,7 +79,7 @@ struct Cfg {
   static constexpr int kBBytes = kKBS * kBTile;
   static constexpr int kSfbBytes = BN < 32 ? BN * 16 : kTokChunk;   // used bytes of a token-scale chunk
   static constexpr int kStageBytes = kABytes + kBBytes + kKBS * (512 + kTokChunk);
-  static constexpr int kSmemBudget = (kCtasPerSm == 1 ? 200 : 96) * 1024;
+  static constexpr int kSmemBudget = (kCtasPerSm == 1 ? 200 : kCtasPerSm == 2 ? 96 : 60) * 1024;
   static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
   static constexpr int kTmemCols = 2 * BN + kSfSlot * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
