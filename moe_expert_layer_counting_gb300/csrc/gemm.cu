@@ -67,6 +67,8 @@ struct Cfg {
   // groups, and an 8-warp epilogue (two warps per TMEM quadrant)
   static constexpr int kKBS = (BN == 16 || BN == 64) ? 1 : 2;
   static constexpr int kCtasPerSm = BN == 16 ? 3 : (BN <= 64 ? 2 : 1);
+  // accumulators in TMEM (two: the epilogue of one item overlaps the MMAs of the next)
+  static constexpr int kAccBufs = 2;
   static constexpr int kSfbGroups = (BN + 127) / 128;       // 128-row groups of token scales
   static constexpr int kTokChunk = 512 * kSfbGroups;        // bytes of one (tile, K block) token-scale chunk
   static constexpr int kSfSlot = 4 + 4 * kSfbGroups;        // TMEM columns of one K block's scales
@@ -81,7 +83,7 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kKBS * (512 + kTokChunk);
   static constexpr int kSmemBudget = (kCtasPerSm == 1 ? 200 : kCtasPerSm == 2 ? 96 : 60) * 1024;
   static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
-  static constexpr int kTmemCols = 2 * BN + kSfSlot * kKBS * kStages;
+  static constexpr int kTmemCols = kAccBufs * BN + kSfSlot * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                          : kTmemCols <= 256 ? 256 : 512;
   // decode-sized tiles: the weights of the next kPrefetchItems work items of
@@ -94,7 +96,7 @@ struct Cfg {
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kKBS * 512;
   static constexpr int kOffEpi = kOffSfb + kStages * kKBS * kTokChunk;   // 4 KB epilogue staging per half
-  // per-item row info, double-buffered by accumulator: pair id [2][BN], weight [2][BN]
+  // per-item row info, double-buffered by item parity: pair id [2][BN], weight [2][BN]
   static constexpr int kOffRow = kOffEpi + 4096 * kEpiHalves;
   static constexpr int kOffBar = kOffRow + 16 * BN;
   static constexpr int kNumBars = 2 * kStages + 5;
@@ -102,6 +104,7 @@ struct Cfg {
   static constexpr int kOffExp = kOffTmemPtr + 64;          // tile_off, counts, offsets: 3*(E+1) ints
   static_assert(kStages >= 2, "need at least two stages");
   static_assert(kTmemCols <= 512, "TMEM budget");
+  static_assert(kTmemAlloc * kCtasPerSm <= 512, "co-resident CTAs share the SM's 512 TMEM columns");
 };
 
 template <int BN>
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
         tc_fence_after();
         if (lane == 0) {
           for (int i = 0; i < nk; ++i) {
-            const uint32_t sf_col = tmem_base + (uint32_t)(2 * BN + C::kSfSlot * (stage * C::kKBS + i));
+            const uint32_t sf_col = tmem_base + (uint32_t)(C::kAccBufs * BN + C::kSfSlot * (stage * C::kKBS + i));
             const uint32_t sfa = smem_u32(smem + C::kOffSfa + (stage * C::kKBS + i) * 512);
             const uint32_t sfb = smem_u32(smem + C::kOffSfb + (stage * C::kKBS + i) * C::kTokChunk);
             tc_cp_32x128b_warpx4(sf_col, make_smem_desc(sfa, 0, 128, kSwizzleNone));
@@ -373,8 +376,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
       if (!ok) break;
       if (lane == 0) tc_commit(&tmem_full[acc]);
       __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1; }
     }
     // all MMAs issued by this thread complete before TMEM is released
     if (lane == 0) tc_commit(mma_done);
@@ -393,13 +395,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     uint16_t *ebuf_h = reinterpret_cast<uint16_t *>(smem + C::kOffEpi + 4096 * eh);
     int acc = 0;
     uint32_t acc_phase = 0;
+    int rb = 0;                              // row-info buffer of this item
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
       const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
       // a half may start this item while the other still reads the previous
-      // item's row info, so it lives in the buffer of this item's accumulator
-      // (reused two items later, after every warp passed this item's vote)
-      int32_t *row_pair = row_pair_buf + acc * BN;
-      float *row_w = row_w_buf + acc * BN;
+      // item's row info, so items alternate between two buffers (one is
+      // reused two items later, after every warp passed this item's vote)
+      int32_t *row_pair = row_pair_buf + rb * BN;
+      float *row_w = row_w_buf + rb * BN;
       if (et < ti.valid) {
         if (PHASE == 1) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
         else row_pair[et] = __ldg(args.perm + ti.s0 + et);
@@ -429,10 +432,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
           for (int j = 0; j < 16; ++j) {
             const float mine = __uint_as_float(v[j]);
             const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
-            if (j >= jbase && j < jbase + 8) {
+            // columns past the tile's tokens hold no pair and are never stored
+            if (j >= jbase && j < jbase + 8 && c0 + j < ti.valid) {
               const float g = is_gate ? mine : other;
               const float u = is_gate ? other : mine;
-              const float h = g / (1.0f + __expf(-g)) * u * row_w[c0 + j];
+              // silu(g) = g / (1 + e^-g); the approximate divide (2 ulp, no
+              // slow path) is far inside the FP8 step of the requantisation
+              const float h = __fdividef(g, 1.0f + __expf(-g)) * u * row_w[c0 + j];
               ebuf_f[j * 64 + feat] = h;
             }
           }
@@ -485,8 +491,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1; }
+      rb ^= 1;
     }
   }
 #ifdef MOE_MXQ_WAIT_STATS
@@ -786,6 +792,16 @@ int launch_prep(const uint8_t *src, const moe_expert_args *a, int KB, uint8_t *c
                     reinterpret_cast<const uint4 *>(a->xq), reinterpret_cast<uint4 *>(xq_pool), (int)(a->H / 16));
 }
 
+// Shared-memory attributes of a GEMM instantiation: its dynamic size and the
+// largest carveout, so that kCtasPerSm CTAs fit on one SM.  (The occupancy
+// calculator reports one CTA per SM for any kernel that allocates TMEM, but
+// CTAs whose allocations fit the SM's 512 columns together are co-resident.)
+template <typename Kernel>
+bool set_gemm_attrs(Kernel kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess &&
+         cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+}
+
 template <int BN>
 int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &lay, cudaStream_t st) {
   using C = Cfg<BN>;
@@ -838,9 +854,7 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
     g.w_codes = a->w1q; g.w_sf = a->w1s; g.b_sf = sfb1;
     set_prefetch(g.KB);
-    if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
+    if (!set_gemm_attrs(expert_gemm_kernel<BN, 1>, sm)) return MOE_ERR_CUDA;
     if (launch_pdl(expert_gemm_kernel<BN, 1>, dim3(grid), dim3(C::kThreads), sm, st, tw1, tb, g) != MOE_OK)
       return MOE_ERR_CUDA;
   }
@@ -857,9 +871,7 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     g.w_codes = a->w2q; g.w_sf = a->w2s; g.b_sf = sfb2;
     set_prefetch(g.KB);
     g.hs_out = nullptr;
-    if (cudaFuncSetAttribute(expert_gemm_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
+    if (!set_gemm_attrs(expert_gemm_kernel<BN, 2>, sm)) return MOE_ERR_CUDA;
     if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(grid), dim3(C::kThreads), sm, st, tw2, th, g) != MOE_OK)
       return MOE_ERR_CUDA;
   }
