@@ -230,7 +230,19 @@ MOE_API int moe_forward(const moe_forward_args *args, cudaStream_t stream);
 
 /* Reads the device status word that kernels write into a workspace (first
  * 4 bytes of any workspace above): MOE_OK, MOE_ERR_TIMEOUT (a bounded
- * device-side wait gave up) or MOE_ERR_DEVICE_INDEX.  Synchronises `stream`. */
+ * device-side wait gave up) or MOE_ERR_DEVICE_INDEX.  Synchronises `stream`.
+ * The int32 words after it: [1] abort flag (raised by the first timeout;
+ * every other wait of the launch then gives up at once), [2] site of the
+ * wait that timed out (1 producer/empty stage, 2 MMA/free accumulator,
+ * 3 MMA/full stage, 4 epilogue/full accumulator, 5 producer drain, 6 MMA
+ * drain, 7 debug wait), [3] its CTA, [4] its loop position.  All are
+ * cleared by each moe_forward / moe_expert_forward call.
+ *
+ * Debug hook for failure-detection tests: with the environment variable
+ * MOE_MXQ_DEBUG_INJECT_WAIT=1 set when a GEMM is launched, the MMA warp of
+ * every CTA with work first waits on a barrier that nothing completes; the
+ * wait gives up after ~10 ms and the launch ends with MOE_ERR_TIMEOUT, site
+ * 7, without faulting and with the context still usable. */
 MOE_API int moe_get_device_status(const void *workspace, cudaStream_t stream, int *out);
 
 /* Human-readable text of a status code (static storage). */

@@ -48,6 +48,7 @@ constexpr int kBM = 128;
 constexpr int kBK = 128;
 constexpr int kChunk = 16;                    // accumulator columns per epilogue step
 constexpr long long kWaitLimit = 2000000000LL;
+constexpr long long kInjectedWaitLimit = 20000000LL;   // ~10 ms: the debug wait's budget
 constexpr int kMaxE = 1024;
 constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in HBM (8 KB)
 
@@ -99,7 +100,7 @@ struct Cfg {
   // per-item row info, double-buffered by item parity: pair id [2][BN], weight [2][BN]
   static constexpr int kOffRow = kOffEpi + 4096 * kEpiHalves;
   static constexpr int kOffBar = kOffRow + 16 * BN;
-  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kNumBars = 2 * kStages + 6;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
   static constexpr int kOffExp = kOffTmemPtr + 64;          // tile_off, counts, offsets: 3*(E+1) ints
   static_assert(kStages >= 2, "need at least two stages");
@@ -116,6 +117,7 @@ struct GemmArgs {
   int E, k, T, H, I;
   int M, K, KB, MT;                 // weight rows / reduction / K blocks / weight tiles per expert
   int prefetch_items;               // L2 prefetch distance of weight tiles, in work items (0 = off)
+  int inject_wait;                  // debug: 1 = the MMA warp first waits on a barrier nothing completes
   uint32_t prefetch_bytes;          // bytes of codes prefetched per work item
   const int32_t *counts, *offsets, *perm;
   const int32_t *tok_pool;          // token of each pool row (GEMM1 gather)
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
   uint64_t *tmem_full = bars + 2 * C::kStages;
   uint64_t *tmem_empty = tmem_full + 2;
   uint64_t *mma_done = tmem_full + 4;
+  uint64_t *never = tmem_full + 5;          // debug wait target: initialised, never arrived on
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::kOffTmemPtr);
   int *vote = reinterpret_cast<int *>(smem + C::kOffTmemPtr + 4);     // one per epilogue warp
   int *tile_off = reinterpret_cast<int *>(smem + C::kOffExp);
@@ -251,6 +254,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
         mbar_init(&tmem_empty[a], C::kEpiWarps);
       }
       mbar_init(mma_done, 1);
+      mbar_init(never, 1);
       fence_mbar_init();
     }
     __syncwarp();
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     // never leave with copies in flight: wait for the last load of each stage
     for (int s = 0; s < C::kStages; ++s)
       if (issued_mask & (1u << s))
-        mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit, kWaitProducerDrain, s);
+        mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit, kWaitProducerDrain, s, false);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     int stage = 0;
@@ -339,6 +343,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
       const uint32_t n_mma = (uint32_t)min(BN, (ti.valid + 15) & ~15);
       if (!__all_sync(0xffffffffu,
                       MXQ_TIMED_WAIT(2, mbar_wait(&tmem_empty[acc], acc_phase ^ 1, status, kWaitLimit, kWaitMmaTmemEmpty, w))))
+        break;
+      // failure-detection test hook: a wait that can only end by its timeout
+      if (args.inject_wait == 1 && w == (int)blockIdx.x &&
+          !__all_sync(0xffffffffu, mbar_wait(never, 0, status, kInjectedWaitLimit, kWaitInjected, w)))
         break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -381,7 +389,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     // all MMAs issued by this thread complete before TMEM is released
     if (lane == 0) tc_commit(mma_done);
     __syncwarp();
-    mbar_wait(mma_done, 0, status, kWaitLimit, kWaitMmaDone, 0);
+    mbar_wait(mma_done, 0, status, kWaitLimit, kWaitMmaDone, 0, false);
   } else {
     // ------------------------------------------------------------ epilogue
     // kEpiWarps warps: quadrant q = warp % 4 of the TMEM lanes; with 8 warps the
@@ -832,6 +840,7 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   const size_t sm = smem_bytes<BN>(E);
   const int grid = num_sms() * C::kCtasPerSm;
   // L2 budget for prefetched weights: ~64 MB over the grid, one or two items ahead
+  if (const char *env = getenv("MOE_MXQ_DEBUG_INJECT_WAIT")) g.inject_wait = atoi(env);
   const auto set_prefetch = [&](int64_t KB) {
     const int64_t item = KB * (kWTileBytes + 512);
     const int64_t budget = (64ll << 20) / grid;

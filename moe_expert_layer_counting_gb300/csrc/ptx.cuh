@@ -75,21 +75,25 @@ enum : int {
   kWaitMmaFull = 3,
   kWaitEpiTmemFull = 4,
   kWaitProducerDrain = 5,
-  kWaitMmaDone = 6
+  kWaitMmaDone = 6,
+  kWaitInjected = 7       // debug: a wait on a barrier that nothing completes
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up after `limit`
-// clock cycles, or as soon as the abort flag is raised, and returns false.
-// On a timeout it raises the abort flag and records the status, the wait
-// site and the loop position `pos` itself.
+// clock cycles, or (honor_abort) as soon as the abort flag is raised, and
+// returns false.  On a timeout it raises the abort flag and records the
+// status, the wait site and the loop position `pos` itself.  Waits for the
+// CTA's own asynchronous copies and MMAs before it exits pass
+// honor_abort = false: those always complete, and the CTA must not release
+// shared memory or TMEM they still write.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *ws_status,
-                                          long long limit, int site = 0, int pos = 0) {
+                                          long long limit, int site = 0, int pos = 0, bool honor_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   volatile int *abort_flag = ws_status + 1;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
+    if (honor_abort && *abort_flag) return false;
     if (clock64() - t0 > limit) {
       if (atomicCAS(ws_status + 2, 0, site) == 0) {
         ws_status[3] = (int)blockIdx.x;
