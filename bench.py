@@ -204,8 +204,7 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.graph(graph, stream=stream):
         forward(torch.cuda.current_stream())
     counts_np = counts.cpu().numpy()
-    # quant, route, permute (count + scatter above 2048 pairs), token scales, GEMM1, GEMM2, combine
-    n_launch_forward = 7 + (1 if T * k > 2048 else 0)
+    n_launch_forward = launches_per_forward(T, H, E, k)
 
     def timed_loop(step_fn, steps):
         evs = []
@@ -405,6 +404,17 @@ def run_reference(args):
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample_txt},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def launches_per_forward(T, H, E, k):
+    """Kernels one moe_forward launches (the dispatch in csrc/api.cu)."""
+    P = T * k
+    permute = 1 if P <= 2048 else 2            # single-block permute, or count + scatter
+    if 1 <= T <= 64 and E <= 256 and P * H <= (4 << 20):
+        return 4                               # front (route + permute + pool cast), GEMM1, GEMM2, combine
+    if P * H <= (16 << 20):
+        return 1 + permute + 1 + 3             # route, permute, pool cast, GEMM1, GEMM2, combine
+    return 1 + 1 + permute + 1 + 3             # quant, route, permute, pool prep, GEMM1, GEMM2, combine
 
 
 def main():

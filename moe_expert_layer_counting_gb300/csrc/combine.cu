@@ -4,8 +4,10 @@
 // DeepEP vs Mega MoE, combine listing: the k BF16 copies of a token are
 // summed in FP32 and cast to BF16 once.  The top-k weight already scaled h
 // before GEMM2, so the sum is unweighted.  Dropped slots (index < 0) are
-// skipped.  One thread owns 8 output values (16-byte loads and stores);
-// the slot sum runs in slot order, so the result is deterministic.
+// skipped.  One thread owns 8 output values (16-byte loads and stores).
+// The slot indices, then the slots' rows, are loaded eight at a time as
+// independent loads (one memory round trip each, not one per slot); the sum
+// still runs in slot order, so the result is deterministic.
 #include <cuda_bf16.h>
 
 #include "host_common.h"
@@ -16,6 +18,7 @@ namespace mxq {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kSlotBatch = 8;              // slots whose loads are in flight together
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4 *__restrict__ yp,
                                                            const int32_t *__restrict__ idx, int64_t T, int k,
@@ -28,14 +31,23 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint4 *__restri
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / H8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      if (__ldg(idx + t * k + j) < 0) continue;
-      const uint4 v = __ldg(yp + j * slot_stride + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int j0 = 0; j0 < k; j0 += kSlotBatch) {
+      bool use[kSlotBatch];
+      uint4 v[kSlotBatch];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[2 * q] += bf16_bits_to_float(w[q] & 0xFFFFu);
-        acc[2 * q + 1] += bf16_bits_to_float(w[q] >> 16);
+      for (int u = 0; u < kSlotBatch; ++u) use[u] = j0 + u < k && __ldg(idx + t * k + j0 + u) >= 0;
+#pragma unroll
+      for (int u = 0; u < kSlotBatch; ++u)
+        if (use[u]) v[u] = __ldg(yp + (j0 + u) * slot_stride + i);
+#pragma unroll
+      for (int u = 0; u < kSlotBatch; ++u) {
+        if (!use[u]) continue;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] += bf16_bits_to_float(w[q] & 0xFFFFu);
+          acc[2 * q + 1] += bf16_bits_to_float(w[q] >> 16);
+        }
       }
     }
     uint32_t o[4];

@@ -102,7 +102,8 @@ struct Cfg {
   static constexpr int kOffBar = kOffRow + 16 * BN;
   static constexpr int kNumBars = 2 * kStages + 6;
   static constexpr int kOffTmemPtr = kOffBar + 8 * kNumBars;
-  static constexpr int kOffExp = kOffTmemPtr + 64;          // tile_off, counts, offsets: 3*(E+1) ints
+  static constexpr int kOffScan = kOffTmemPtr + 64;         // block-scan scratch: warp sums + total
+  static constexpr int kOffExp = kOffScan + 64;             // tile_off, counts, offsets: 3*(E+1) ints
   static_assert(kStages >= 2, "need at least two stages");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kTmemAlloc * kCtasPerSm <= 512, "co-resident CTAs share the SM's 512 TMEM columns");
@@ -144,26 +145,6 @@ __device__ __forceinline__ void load_expert_table(const int32_t *counts, const i
     if (e < E) cnt_sm[e] = __ldg(counts + e);
     off_sm[e] = __ldg(offsets + e);
   }
-}
-
-// Exclusive prefix of ceil(cnt_sm[e] / BN) by one warp, from shared memory.
-template <int BN>
-__device__ void scan_tile_map(const int *cnt_sm, int E, int *tile_off) {
-  const int lane = threadIdx.x & 31;
-  int carry = 0;
-  for (int b = 0; b < E; b += 32) {
-    const int e = b + lane;
-    const int nt = e < E ? (cnt_sm[e] + BN - 1) / BN : 0;
-    int inc = nt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += n;
-    }
-    if (e < E) tile_off[e] = carry + inc - nt;
-    carry += __shfl_sync(0xffffffffu, inc, 31);
-  }
-  if (lane == 0) tile_off[E] = carry;
 }
 
 template <int BN>
@@ -266,7 +247,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
   pdl_wait();
   load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm);
   __syncthreads();
-  if (warp == 0) scan_tile_map<BN>(cnt_sm, args.E, tile_off);
+  block_tile_map<C::kThreads>(cnt_sm, args.E, BN, tile_off, reinterpret_cast<int *>(smem + C::kOffScan),
+                              reinterpret_cast<int *>(smem + C::kOffScan) + 15);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -545,7 +527,8 @@ __global__ void __launch_bounds__(256) prep_pool_kernel(const uint8_t *__restric
   pdl_wait();
   load_expert_table(counts, offsets, E, cnt_sm, off_sm);
   __syncthreads();
-  if (threadIdx.x < 32) scan_tile_map<BN>(cnt_sm, E, tile_off);
+  __shared__ int scan_scratch[9];
+  block_tile_map<256>(cnt_sm, E, BN, tile_off, scan_scratch, scan_scratch + 8);
   __syncthreads();
   const int P = off_sm[E];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -603,7 +586,8 @@ __global__ void __launch_bounds__(256) pool_cast_kernel(const uint4 *__restrict_
   pdl_wait();
   load_expert_table(counts, offsets, E, cnt_sm, off_sm);
   __syncthreads();
-  if (threadIdx.x < 32) scan_tile_map<BN>(cnt_sm, E, tile_off);
+  __shared__ int scan_scratch[9];
+  block_tile_map<256>(cnt_sm, E, BN, tile_off, scan_scratch, scan_scratch + 8);
   __syncthreads();
   const int P = off_sm[E];
   const int H8 = H / 8, KB = H / 128;
@@ -645,9 +629,11 @@ __global__ void __launch_bounds__(256) pool_cast_kernel(const uint4 *__restrict_
 // Small problems in one launch.  Every CTA routes all T tokens and builds the
 // whole counting-sort permutation in shared memory -- the same result in every
 // CTA, so no grid-wide synchronisation is needed -- CTA 0 writes the routing
-// and permute outputs, and every CTA then casts its share of the pool rows
-// exactly as pool_cast_kernel does.  Used for T <= 64, E <= 256 (a few KB of
-// logits per CTA).
+// and permute outputs, and every CTA then casts its columns (gpc 32-value
+// groups) of every pool row as pool_cast_kernel does.  The x values of those
+// columns for all T tokens are read into shared memory before routing starts,
+// so that the cast waits on no global load.  Used for T <= 64, E <= 256 (a
+// few KB of logits per CTA).
 constexpr int kFrontThreads = 256;
 constexpr int kFrontMaxT = 64, kFrontMaxE = 256;
 
@@ -657,12 +643,15 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts_out,
     int32_t *__restrict__ offsets_out, int32_t *__restrict__ perm_out, int32_t *__restrict__ inv_perm_out,
     uint8_t *__restrict__ chunks, int32_t *__restrict__ tok_pool, float *__restrict__ w_pool,
-    uint2 *__restrict__ xq_pool) {
+    uint2 *__restrict__ xq_pool, int gpc) {
   constexpr int kW = kFrontThreads / 32;
   extern __shared__ __align__(16) unsigned char fsm[];
   const int P = T * k;
-  float *rows = reinterpret_cast<float *>(fsm);                        // [kW][E]
-  int *idx_sm = reinterpret_cast<int *>(rows + kW * E);                // [P]
+  const int H8 = H / 8, KB = H / 128;
+  const int cc0 = blockIdx.x * gpc * 4;                                // first 8-value column of this CTA
+  const int ncols = max(0, min(gpc * 4, H8 - cc0));
+  uint4 *xs = reinterpret_cast<uint4 *>(fsm);                          // [T][gpc * 4]
+  int *idx_sm = reinterpret_cast<int *>(xs + (size_t)T * gpc * 4);     // [P]
   float *w_sm = reinterpret_cast<float *>(idx_sm + P);                 // [P]
   int *perm_sm = reinterpret_cast<int *>(w_sm + P);                    // [P]
   int *cnt = perm_sm + P;                                              // [E+1]
@@ -676,14 +665,19 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
   const bool writer = blockIdx.x == 0;
   pdl_launch_dependents();
   pdl_wait();
+  // 0. this CTA's columns of x (consumed in step 3): the first 16 bytes per
+  // thread are loaded into a register here and land in shared memory after
+  // routing, so that their latency overlaps the logits loads
+  const int nx = T * ncols;
+  uint4 xv = make_uint4(0, 0, 0, 0);
+  if (tid < nx) xv = __ldg(x + (size_t)(tid / ncols) * H8 + cc0 + tid % ncols);
+  for (int i = tid + kFrontThreads; i < nx; i += kFrontThreads)
+    xs[i] = __ldg(x + (size_t)(i / ncols) * H8 + cc0 + i % ncols);
   // 1. routing of every token, one warp per token
   for (int t = warp; t < T; t += kW) {
-    float *row = rows + warp * E;
-    for (int e = lane; e < E; e += 32) row[e] = __ldg(logits + (size_t)t * E + e);
-    __syncwarp();
     int my_idx;
     float my_w;
-    warp_route_token(row, E, k, lane, &my_idx, &my_w);
+    warp_route_token<kFrontMaxE / 32>(logits + (size_t)t * E, E, k, lane, &my_idx, &my_w);
     if (lane < k) {
       idx_sm[t * k + lane] = my_idx;
       w_sm[t * k + lane] = my_w;
@@ -694,6 +688,7 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
     }
     __syncwarp();
   }
+  if (tid < nx) xs[tid] = xv;
   for (int e = tid; e <= E; e += kFrontThreads) cnt[e] = 0;
   __syncthreads();
   // 2. count -> prefix -> stable scatter
@@ -713,26 +708,25 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
     if (writer) offsets_out[E] = *total;
   }
   __syncthreads();
-  if (warp == 0) scan_tile_map<BN>(cnt, E, tile_off);
+  block_tile_map<kFrontThreads>(cnt, E, BN, tile_off, warp_sums, total);
   block_stable_ranks<kFrontThreads>([&](int64_t p) { return idx_sm[p]; }, 0, P, E, base, wc,
                                     writer ? perm_out : nullptr, writer ? inv_perm_out : nullptr, perm_sm);
-  // 3. this CTA's share of the pool rows
-  const int H8 = H / 8, KB = H / 128;
-  const int64_t items = (int64_t)P * H8;
-  const int64_t stride = (int64_t)gridDim.x * kFrontThreads;
-  for (int64_t b0 = (int64_t)blockIdx.x * kFrontThreads; b0 < items; b0 += stride) {
-    const int64_t i = b0 + tid;
+  // 3. this CTA's columns of every pool row (four lanes per 32-value group)
+  const int items = P * ncols;
+  for (int b0 = 0; b0 < items; b0 += kFrontThreads) {
+    const int i = b0 + tid;
     const bool valid = i < items;
-    int sr = 0, c = 0, t = 0, pp = 0;
+    int sr = 0, cl = 0, t = 0, pp = 0;
     if (valid) {
-      sr = (int)(i / H8);
-      c = (int)(i - (int64_t)sr * H8);
+      sr = i / ncols;
+      cl = i - sr * ncols;
       pp = perm_sm[sr];
       t = pp / k;
     }
     uint8_t sb;
-    const uint2 codes = cast8_e4m3(valid ? __ldg(x + (size_t)t * H8 + c) : make_uint4(0, 0, 0, 0), valid, &sb);
+    const uint2 codes = cast8_e4m3(valid ? xs[t * ncols + cl] : make_uint4(0, 0, 0, 0), valid, &sb);
     if (!valid) continue;
+    const int c = cc0 + cl;
     xq_pool[(size_t)sr * H8 + c] = codes;
     if ((c & 3) == 0) {
       int lo = 0, hi = E;
@@ -753,25 +747,27 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
   }
 }
 
-size_t front_smem(int T, int E, int k) {
+size_t front_smem(int T, int E, int k, int gpc) {
   const int P = T * k;
-  return (size_t)(kFrontThreads / 32) * E * 4 + (size_t)3 * P * 4 + (size_t)3 * (E + 1) * 4 + (size_t)E * 4 +
-         (kFrontThreads / 32) * 4 + 16 + (size_t)(kFrontThreads / 32) * E * 2;
+  return (size_t)T * gpc * 64 + (size_t)3 * P * 4 +
+         (size_t)3 * (E + 1) * 4 + (size_t)E * 4 + (kFrontThreads / 32) * 4 + 16 +
+         (size_t)(kFrontThreads / 32) * E * 2;
 }
 
 template <int BN>
 int launch_front_t(const moe_expert_args *a, const uint16_t *x, const float *logits, int32_t *idx, float *wts,
                    int32_t *inv_perm, char *ws, const ExpertWs &lay, cudaStream_t st) {
-  const int64_t P = a->T * a->k;
-  const int64_t blocks = ceil_div(P * (a->H / 8), kFrontThreads);
+  // one CTA per 32-value column group of the pool rows, at most two per SM
+  const int groups = (int)(a->H / 32);
   const int cap = num_sms() * 2;
-  const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
-  return launch_pdl(front_kernel<BN>, dim3(grid), dim3(kFrontThreads), front_smem((int)a->T, a->E, a->k), st, logits,
-                    reinterpret_cast<const uint4 *>(x), (int)a->T, a->E, a->k, (int)a->H, idx, wts,
+  const int grid = groups < cap ? groups : cap;
+  const int gpc = (groups + grid - 1) / grid;
+  return launch_pdl(front_kernel<BN>, dim3(grid), dim3(kFrontThreads), front_smem((int)a->T, a->E, a->k, gpc), st,
+                    logits, reinterpret_cast<const uint4 *>(x), (int)a->T, a->E, a->k, (int)a->H, idx, wts,
                     const_cast<int32_t *>(a->counts), const_cast<int32_t *>(a->offsets),
                     const_cast<int32_t *>(a->perm), inv_perm, reinterpret_cast<uint8_t *>(ws + lay.sfb1),
                     reinterpret_cast<int32_t *>(ws + lay.tok_pool), reinterpret_cast<float *>(ws + lay.w_pool),
-                    reinterpret_cast<uint2 *>(ws + lay.xq_pool));
+                    reinterpret_cast<uint2 *>(ws + lay.xq_pool), gpc);
 }
 
 template <int BN>

@@ -7,44 +7,68 @@
 
 namespace mxq {
 
-__device__ __forceinline__ bool route_better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
+// Order-preserving key of a finite logit (larger key = larger value); -0.0
+// takes +0.0's key, so that equal values differ only by expert index.
+__device__ __forceinline__ uint32_t route_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float route_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
 // Softmax top-k routing of one token by one warp (MonoMoe kernel -- design,
-// section 1).  `row` is the token's E logits in this warp's shared memory (it
-// is consumed: chosen entries are overwritten).  Selection ranks the raw
-// logits, equal logits go to the lower expert index, output in descending
-// order; w_j = exp(l_j - l_max) / sum over the k chosen.  Lane j < k returns
-// the j-th choice in *idx_out / *w_out.
-__device__ __forceinline__ void warp_route_token(float *row, int E, int k, int lane, int *idx_out, float *w_out) {
-  float my_val = 0.f;
-  int my_idx = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float v = row[e];
-      if (route_better(v, e, bv, bi)) { bv = v; bi = e; }
-    }
+// section 1), straight from the token's E logits in global memory.
+// Selection ranks the raw logits, equal logits go to the lower expert index,
+// output in descending order; w_j = exp(l_j - l_max) / sum over the k chosen.
+// Lane l holds the keys of experts l + 32 u (u < NV) in registers; each of
+// the k rounds takes every lane's best remaining key, the warp maximum of
+// those (redux) and, among the lanes that hold it, the lowest expert index
+// (redux again); the owner clears that key.  Lane j < k returns the j-th
+// choice in *idx_out / *w_out.  E <= 32 * NV; k <= min(E, 32).
+template <int NV>
+__device__ __forceinline__ void warp_route_token(const float *__restrict__ src, int E, int k, int lane,
+                                                 int *idx_out, float *w_out) {
+  uint32_t key[NV];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (route_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == j) { my_val = bv; my_idx = bi; }
-    if (lane == (bi & 31)) row[bi] = -INFINITY;     // taken (logits are finite)
-    __syncwarp();
+  for (int u = 0; u < NV; ++u) {
+    const int e = lane + 32 * u;
+    key[u] = e < E ? route_key(__ldg(src + e)) : 0u;    // 0: no expert (below every finite logit's key)
   }
+  int my_idx = 0;
+  uint32_t my_key = 0;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0;
+    int bu = 0;
+#pragma unroll
+    for (int u = 0; u < NV; ++u)
+      if (key[u] > bk) { bk = key[u]; bu = u; }           // ascending u: ties keep the lower index
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const int e = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)(lane + 32 * bu) : 0xffffffffu);
+    if (lane == j) { my_idx = e; my_key = kmax; }
+#pragma unroll
+    for (int u = 0; u < NV; ++u)
+      if (lane == (e & 31) && u == (e >> 5)) key[u] = 0;
+  }
+  const float my_val = route_key_value(my_key);
   const float lmax = __shfl_sync(0xffffffffu, my_val, 0);
   const float ex = lane < k ? expf(my_val - lmax) : 0.f;
   float sum = ex;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   *idx_out = my_idx;
-  *w_out = __fdiv_rn(ex, sum);
+  *w_out = lane < k ? __fdiv_rn(ex, sum) : 0.f;
 }
+
+// Exclusive prefix of ceil(cnt[e] / bn) over e < E into tile_off[0..E] (the
+// first token tile of each expert; tile_off[E] = all tiles), by all NT
+// threads of the block: each thread sums a contiguous run of experts, one
+// block scan joins the runs.  warp_sums: NT/32 ints, total: 1 int.  The
+// caller synchronises before reading tile_off.
+template <int NT>
+__device__ __forceinline__ void block_tile_map(const int *cnt, int E, int bn, int *tile_off, int *warp_sums,
+                                               int *total);
 
 // Exclusive scan of one value per thread over a block of NT threads; returns
 // the prefix and writes the block total to *total.  warp_sums: NT/32 ints.
@@ -73,6 +97,21 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
   }
   __syncthreads();
   return inc - v + warp_sums[warp];
+}
+
+template <int NT>
+__device__ __forceinline__ void block_tile_map(const int *cnt, int E, int bn, int *tile_off, int *warp_sums,
+                                               int *total) {
+  const int per = (E + NT - 1) / NT;
+  const int lo = min(E, (int)threadIdx.x * per), hi = min(E, lo + per);
+  int sum = 0;
+  for (int e = lo; e < hi; ++e) sum += (cnt[e] + bn - 1) / bn;
+  int run = block_exclusive_scan<NT>(sum, warp_sums, total);
+  for (int e = lo; e < hi; ++e) {
+    tile_off[e] = run;
+    run += (cnt[e] + bn - 1) / bn;
+  }
+  if (threadIdx.x == 0) tile_off[E] = *total;
 }
 
 // Stable ranks of pairs [lo, hi) inside their experts, NT pairs at a time

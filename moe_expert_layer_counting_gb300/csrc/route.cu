@@ -21,18 +21,14 @@ constexpr int kMaxE = 1024;
 __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restrict__ logits, int64_t T, int E,
                                                             int k, int32_t *__restrict__ idx,
                                                             float *__restrict__ w) {
-  extern __shared__ float sm[];                       // kWarps x E logits
   pdl_launch_dependents();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float *row = sm + (size_t)warp * E;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < T; t += (int64_t)gridDim.x * kWarps) {
-    const float *src = logits + t * E;
-    for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
-    __syncwarp();
     int my_idx;
     float my_w;
-    warp_route_token(row, E, k, lane, &my_idx, &my_w);
+    if (E <= 256) warp_route_token<8>(logits + t * E, E, k, lane, &my_idx, &my_w);
+    else warp_route_token<kMaxE / 32>(logits + t * E, E, k, lane, &my_idx, &my_w);
     if (lane < k) {
       idx[t * k + lane] = my_idx;
       w[t * k + lane] = my_w;
@@ -48,13 +44,7 @@ int launch_route(const float *logits, int64_t T, int E, int k, int32_t *idx, flo
   const int64_t blocks = ceil_div(T, kWarps);
   const int64_t cap = (int64_t)num_sms() * 8;
   const int grid = (int)(blocks < cap ? blocks : cap);
-  const size_t smem = (size_t)kWarps * E * sizeof(float);
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
-  return launch_pdl(route_kernel, dim3(grid), dim3(kWarps * 32), smem, st, logits, T, E, k, idx, w);
+  return launch_pdl(route_kernel, dim3(grid), dim3(kWarps * 32), 0, st, logits, T, E, k, idx, w);
 }
 
 }  // namespace mxq
