@@ -98,6 +98,11 @@ def _route_cases():
     out.append(("ties", torch.from_numpy(pool[g.integers(0, 6, (300, 64))]), 6))
     out.append(("wide_E", torch.randn(50, 1024, generator=torch.Generator().manual_seed(2)), 32))
     out.append(("k1", torch.randn(40, 10, generator=torch.Generator().manual_seed(3)), 1))
+    # E just above one and eight warp widths (register key arrays of 8 and 32 per lane)
+    out.append(("E33", torch.randn(70, 33, generator=torch.Generator().manual_seed(4)), 32))
+    out.append(("E257", torch.randn(70, 257, generator=torch.Generator().manual_seed(5)), 8))
+    ties = torch.from_numpy(pool[g.integers(0, 6, (64, 300))])
+    out.append(("ties_E300", ties, 32))
     return out
 
 

@@ -1,0 +1,49 @@
+"""moe_forward across shapes that take each dispatch path, compared in full
+with the oracle.
+
+moe_forward picks one of three front ends from the problem size: the fused
+small-problem kernel (T <= 64, E <= 256, T*k*H <= 4M), routing + permute + a
+pool cast (P*H <= 16M), or routing + permute + activation cast + pool copy
+(larger), and the token tile from the mean pairs per routed expert.  The
+shapes below are small enough for the float64 oracle, with ragged counts,
+E not a multiple of 32, a single token, k = 1, and a few thousand pairs."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import moe as O
+from tests import helpers as Hp
+from tests.test_gpu_expert import Setup, _forward
+
+pytestmark = pytest.mark.gpu
+
+# name: (T, H, I, E, k) -- expected path and tile in the comment
+SHAPES = {
+    "one_token": (1, 256, 128, 5, 3),            # front kernel, 16-token tiles
+    "odd_E": (37, 384, 128, 77, 5),             # front kernel, E not a multiple of 32
+    "E256_k8": (64, 256, 128, 256, 8),          # front kernel at its largest T and E
+    "k1": (40, 512, 256, 10, 1),                # front kernel, k = 1 (weight 1)
+    "pool_cast": (100, 256, 128, 24, 4),        # T > 64: routing + permute + pool cast
+    "wide_H_front": (3, 7168, 128, 9, 2),       # front kernel, 224 column groups
+    "large_path": (2048, 1024, 128, 64, 8),     # P*H > 16M: activation cast + pool copy, 224-token tiles
+}
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return Hp.lib()
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_forward_shape(B, name):
+    T, H, I, E, k = SHAPES[name]
+    wl = W.Workload(name, T=T, H=H, I=I, E=E, k=k, sigma=0.02, seed=11 + len(name))
+    st = Setup(B, wl, weight_device="cuda")
+    y_g, _ = _forward(B, st)
+    ref = O.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, k)
+    Hp.assert_bf16_close(y_g, ref["y"], what=name)
+    if k == 1:
+        assert np.all(st.w_ref == 1.0)
