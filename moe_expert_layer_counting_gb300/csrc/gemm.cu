@@ -119,6 +119,11 @@ struct GemmArgs {
   int M, K, KB, MT;                 // weight rows / reduction / K blocks / weight tiles per expert
   int prefetch_items;               // L2 prefetch distance of weight tiles, in work items (0 = off)
   int inject_wait;                  // debug: 1 = the MMA warp first waits on a barrier nothing completes
+  // GEMM2 launched right after GEMM1 in the same call: the expert table and
+  // the first stages' weight loads are issued before griddepcontrol.wait
+  // (GEMM1 signals its dependents only after its own wait, so the routing
+  // outputs are final by then; weights are never written by a kernel)
+  int early_weights;
   uint32_t prefetch_bytes;          // bytes of codes prefetched per work item
   const int32_t *counts, *offsets, *perm;
   const int32_t *tok_pool;          // token of each pool row (GEMM1 gather)
@@ -140,10 +145,15 @@ struct TileInfo {
 // counts/offsets -> shared memory with independent loads by every thread of
 // the block (no chain of dependent global loads in the prologue).
 __device__ __forceinline__ void load_expert_table(const int32_t *counts, const int32_t *offsets, int E,
-                                                  int *cnt_sm, int *off_sm) {
+                                                  int *cnt_sm, int *off_sm, bool from_l2 = false) {
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    if (e < E) cnt_sm[e] = __ldg(counts + e);
-    off_sm[e] = __ldg(offsets + e);
+    if (from_l2) {
+      if (e < E) cnt_sm[e] = __ldcg(counts + e);
+      off_sm[e] = __ldcg(offsets + e);
+    } else {
+      if (e < E) cnt_sm[e] = __ldg(counts + e);
+      off_sm[e] = __ldg(offsets + e);
+    }
   }
 }
 
@@ -218,7 +228,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
   int n_items = 0;
 #endif
 
-  pdl_launch_dependents();
+  if (PHASE != 1) pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
@@ -243,9 +253,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     tmem_relinquish();
   }
   // everything above touches no global memory; the previous kernel's outputs
-  // (counts, offsets, pool rows, scales) are read only after this point
-  pdl_wait();
-  load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm);
+  // (counts, offsets, pool rows, scales) are read only after this point --
+  // except, with early_weights, the routing outputs of the kernel before the
+  // previous one (L2 reads) and static weights (producer, below)
+  const bool early = PHASE == 2 && args.early_weights != 0;
+  if (!early) pdl_wait();
+  if (PHASE == 1) pdl_launch_dependents();
+  load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm, early);
   __syncthreads();
   block_tile_map<C::kThreads>(cnt_sm, args.E, BN, tile_off, reinterpret_cast<int *>(smem + C::kOffScan),
                               reinterpret_cast<int *>(smem + C::kOffScan) + 15);
@@ -275,32 +289,53 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
       prefetch_l2_bulk(args.w_sf + first * 512, (uint32_t)args.KB * 512);
     };
     for (int i = 0; i <= pf_items && pf_items > 0; ++i) prefetch_item(blockIdx.x + i * gridDim.x);
+    // one stage = the weight part (codes + weight scales, static data) and the
+    // token part (pool rows or h, token scales, written by earlier kernels);
+    // the stage's barrier expects both
+    auto issue_weights = [&](int st, int kb, int nk, int wtile) {
+      const uint32_t sfb_bytes = (uint32_t)((nk - 1) * C::kTokChunk + C::kSfbBytes);
+      // the weight box always spans kKBS tiles (rows past the tensor read as zeros);
+      // the FP4-unpacking load completes the packed byte count
+      mbar_arrive_expect_tx(&full[st], (uint32_t)(C::kKBS * kWTileBytes + nk * C::kBTile + nk * 512) + sfb_bytes);
+      tma_load_2d(smem + C::kOffA + st * C::kABytes, &tmap_w, &full[st], 0, (wtile + kb) * kBM);
+      bulk_load(smem + C::kOffSfa + st * C::kKBS * 512, args.w_sf + ((size_t)wtile + kb) * 512, nk * 512, &full[st]);
+    };
+    auto issue_tokens = [&](int st, int kb, int nk, const TileInfo &ti) {
+      const uint32_t sfb_bytes = (uint32_t)((nk - 1) * C::kTokChunk + C::kSfbBytes);
+      const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB + kb) * C::kTokChunk;
+      bulk_load(smem + C::kOffSfb + st * C::kKBS * C::kTokChunk, sfb_src, sfb_bytes, &full[st]);
+      unsigned char *b_dst = smem + C::kOffB + st * C::kBBytes;
+      for (int i = 0; i < nk; ++i) tma_load_2d(b_dst + i * C::kBTile, &tmap_b, &full[st], (kb + i) * kBK, ti.s0);
+    };
+    // early_weights: the first item's first stages get their weight part now,
+    // their token part after griddepcontrol.wait (all stages are free here)
+    int pre = 0;
+    if (early) {
+      if (blockIdx.x < total_work) {
+        const TileInfo t0 = decode_work<BN>(blockIdx.x, args.MT, args.E, tile_off, cnt_sm, off_sm);
+        const int wtile0 = (t0.e * args.MT + t0.mt) * args.KB;
+        for (; pre < C::kStages && pre * C::kKBS < args.KB; ++pre)
+          if (lane == 0) issue_weights(pre, pre * C::kKBS, min(C::kKBS, args.KB - pre * C::kKBS), wtile0);
+        __syncwarp();
+      }
+      pdl_wait();
+    }
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
       const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
       if (pf_items > 0 && w != (int)blockIdx.x) prefetch_item(w + pf_items * (int)gridDim.x);
       const int wtile = (ti.e * args.MT + ti.mt) * args.KB;        // first weight tile of this item
-      const uint8_t *sfa_src = args.w_sf + (size_t)wtile * 512;
-      const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB) * C::kTokChunk;
       for (int kb = 0; kb < args.KB; kb += C::kKBS) {
         const int nk = min(C::kKBS, args.KB - kb);                   // K blocks in this stage
-        if (!__all_sync(0xffffffffu,
+        const bool pre_armed = w == (int)blockIdx.x && kb < pre * C::kKBS;
+        if (!pre_armed &&
+            !__all_sync(0xffffffffu,
                         MXQ_TIMED_WAIT(0, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb)))) {
           ok = false;
           break;
         }
-        unsigned char *a_dst = smem + C::kOffA + stage * C::kABytes;
-        unsigned char *b_dst = smem + C::kOffB + stage * C::kBBytes;
         if (lane == 0) {
-          // the weight box always spans kKBS tiles (rows past the tensor read as zeros);
-          // the FP4-unpacking load completes the packed byte count
-          const uint32_t sfb_bytes = (uint32_t)((nk - 1) * C::kTokChunk + C::kSfbBytes);
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(C::kKBS * kWTileBytes + nk * C::kBTile + nk * 512) + sfb_bytes);
-          tma_load_2d(a_dst, &tmap_w, &full[stage], 0, (wtile + kb) * kBM);
-          bulk_load(smem + C::kOffSfa + stage * C::kKBS * 512, sfa_src + (size_t)kb * 512, nk * 512, &full[stage]);
-          bulk_load(smem + C::kOffSfb + stage * C::kKBS * C::kTokChunk, sfb_src + (size_t)kb * C::kTokChunk, sfb_bytes,
-                    &full[stage]);
-          for (int i = 0; i < nk; ++i)
-            tma_load_2d(b_dst + i * C::kBTile, &tmap_b, &full[stage], (kb + i) * kBK, ti.s0);
+          if (!pre_armed) issue_weights(stage, kb, nk, wtile);
+          issue_tokens(stage, kb, nk, ti);
         }
         __syncwarp();
         issued_mask |= 1u << stage;
@@ -314,6 +349,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
         mbar_wait(&full[s], (issued_phase >> s) & 1u, status, kWaitLimit, kWaitProducerDrain, s, false);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    if (early) pdl_wait();
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -377,6 +413,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     // kEpiWarps warps: quadrant q = warp % 4 of the TMEM lanes; with 8 warps the
     // two halves take alternate 16-column chunks, each with its own staging
     // buffer and named barrier.
+    if (early) pdl_wait();
     const int q = warp & 3;                  // TMEM lane quadrant of this warp
     const int eh = (warp - 2) >> 2;          // epilogue half
     const int et = threadIdx.x - 64;         // 0 .. 32 * kEpiWarps - 1
@@ -874,6 +911,7 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     if (!ok) return MOE_ERR_CUDA;
     g.M = (int)a->H; g.K = (int)a->I; g.KB = (int)(a->I / 128); g.MT = (int)(a->H / 128);
     g.w_codes = a->w2q; g.w_sf = a->w2s; g.b_sf = sfb2;
+    g.early_weights = (phases & MOE_PHASE_GEMM1) ? 1 : 0;
     set_prefetch(g.KB);
     g.hs_out = nullptr;
     if (!set_gemm_attrs(expert_gemm_kernel<BN, 2>, sm)) return MOE_ERR_CUDA;
