@@ -85,21 +85,36 @@ def dequant_e2m1(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
 
 # ---------------------------------------------------------------- routing
 
-def route_topk(logits_f32: np.ndarray, k: int):
-    """Softmax top-k routing with renormalisation.
+ROUTE_SCORINGS = ("softmax", "sigmoid", "raw")
 
-    MonoMoe kernel -- design, section 1 (phase 1: softmax top-K with optional
-    renormalisation); the MegaMoE test draws ``scores = randn`` and takes
-    ``torch.topk`` (Counting Sort / Bucketization in DeepGEMM Mega MoE,
-    section 7.1).  Ranking the raw logits gives the same set as ranking the
-    softmax probabilities, without ties that rounding of the probabilities
-    could create.  Equal logits: the lower expert index wins; output order is
-    descending logit (lower index first on ties).
 
-    Weights: w_j = exp(l_j - l_max) / sum_{i in selected} exp(l_i - l_max), in
-    float64, stored as float32 (nearest even).  The full softmax denominator
-    cancels in the renormalisation.
+def route_topk(logits_f32: np.ndarray, k: int, scoring: str = "softmax", renormalize: bool = True):
+    """Top-k routing: softmax (default) or sigmoid scores, optional renormalisation.
+
+    MonoMoe kernel -- design, section 1 (phase 1: softmax or sigmoid top-K
+    with optional renormalisation); the MegaMoE test draws ``scores = randn``
+    and takes ``torch.topk`` of them, the raw scores becoming the weights
+    (Counting Sort / Bucketization in DeepGEMM Mega MoE, section 7.1):
+    scoring = "raw", no renormalisation.
+
+    Selection ranks the raw logits: softmax and sigmoid are increasing, so
+    the set is the same as ranking the scores, without the ties that
+    rounding of the scores could create.  Equal logits: the lower expert
+    index wins; output order is descending logit (lower index first on ties).
+
+    Weights, in float64, stored as float32 (nearest even), with l_max the
+    largest logit of the token and S the k selected experts:
+      softmax, renormalised:  w_j = exp(l_j - l_max) / sum_{i in S} exp(l_i - l_max)
+                              (the full softmax denominator cancels)
+      softmax, not renorm.:   w_j = exp(l_j - l_max) / sum_{all e} exp(l_e - l_max)
+      sigmoid, renormalised:  w_j = s_j / sum_{i in S} s_i,  s = 1 / (1 + exp(-l))
+      sigmoid, not renorm.:   w_j = s_j
+      raw (not renorm.):      w_j = l_j
     """
+    if scoring not in ROUTE_SCORINGS:
+        raise ValueError(f"unknown scoring {scoring!r}")
+    if scoring == "raw" and renormalize:
+        raise ValueError("raw scores are not renormalised")
     logits = np.asarray(logits_f32, dtype=np.float32)
     T, E = logits.shape
     assert 1 <= k <= E
@@ -111,10 +126,18 @@ def route_topk(logits_f32: np.ndarray, k: int):
         l = logits[t].astype(np.float64)
         order = np.argsort(-l, kind="stable")       # descending value, ascending index on ties
         sel = order[:k]
-        lmax = l[sel[0]]
-        ex = np.exp(l[sel] - lmax)
         idx[t] = sel
-        w[t] = (ex / ex.sum()).astype(np.float32)
+        if scoring == "softmax":
+            lmax = l[sel[0]]
+            ex = np.exp(l[sel] - lmax)
+            denom = ex.sum() if renormalize else np.exp(l - lmax).sum()
+            wt = ex / denom
+        elif scoring == "sigmoid":
+            sg = 1.0 / (1.0 + np.exp(-l[sel]))
+            wt = sg / sg.sum() if renormalize else sg
+        else:
+            wt = l[sel]
+        w[t] = wt.astype(np.float32)
     return idx, w
 
 
