@@ -95,12 +95,34 @@ MOE_API int mxq_quantize_act(const uint16_t *x, int64_t rows, int64_t K,
 MOE_API int mxq_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int64_t K, int layout,
                         uint8_t *q, uint8_t *s, cudaStream_t stream);
 
+/* Routing modes: the score (low two bits) and MOE_ROUTE_NO_RENORM.  0 is
+ * the default, softmax renormalised over the k chosen.  Raw scores are never
+ * renormalised (MOE_ROUTE_RAW with or without the flag). */
+enum moe_route_mode {
+    MOE_ROUTE_SOFTMAX = 0,       /* softmax over the E logits                  */
+    MOE_ROUTE_SIGMOID = 1,       /* s = 1 / (1 + exp(-l)) per expert           */
+    MOE_ROUTE_RAW = 2,           /* the logits themselves (MegaMoE test)       */
+    MOE_ROUTE_NO_RENORM = 4      /* flag: keep the scores of the k chosen as is */
+};
+
 /* Router: per token, the k largest logits (equal logits: lower expert index
- * first), in descending order, and weights softmax-renormalised over the k
- * chosen: w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max).
- * MonoMoe kernel -- design, section 1 (phase 1: softmax top-K, renormalise).
- * logits [T][E] f32 (finite); topk_idx [T][k] i32; topk_w [T][k] f32. */
+ * first; -0.0 equals +0.0), in descending order, and their weights.  Every
+ * score is an increasing function of the logit, so ranking the logits
+ * selects the k best scores.  With l_max the top logit and S the k chosen:
+ *   softmax:              w_j = exp(l_j - l_max) / sum_{i in S} exp(l_i - l_max)
+ *   softmax | NO_RENORM:  w_j = exp(l_j - l_max) / sum_{all e} exp(l_e - l_max)
+ *   sigmoid:              w_j = s_j / sum_{i in S} s_i
+ *   sigmoid | NO_RENORM:  w_j = s_j
+ *   raw:                  w_j = l_j
+ * MonoMoe kernel -- design, section 1 (phase 1: softmax or sigmoid top-K with
+ * optional renormalisation); raw scores as the MegaMoE test's topk of randn
+ * scores (Counting Sort / Bucketization in DeepGEMM Mega MoE, section 7.1).
+ * logits [T][E] f32 (finite); topk_idx [T][k] i32; topk_w [T][k] f32.
+ * 1 <= k <= min(E, 32), E <= 1024; an unknown mode is MOE_ERR_INVALID_ARG.
+ * moe_route_topk is moe_route_topk_ex with mode MOE_ROUTE_SOFTMAX. */
 MOE_API int moe_route_topk(const float *logits, int64_t T, int32_t E, int32_t k,
+                   int32_t *topk_idx, float *topk_w, cudaStream_t stream);
+MOE_API int moe_route_topk_ex(const float *logits, int64_t T, int32_t E, int32_t k, int32_t mode,
                    int32_t *topk_idx, float *topk_w, cudaStream_t stream);
 
 /* Counting-sort permute of the P = T*k (token, slot) pairs, pair id
@@ -223,6 +245,7 @@ typedef struct moe_forward_args {
     int32_t tile_n;
     void *workspace;
     size_t workspace_bytes;
+    int32_t route_mode;     /* enum moe_route_mode; 0 = softmax, renormalised */
 } moe_forward_args;
 
 MOE_API size_t moe_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k);

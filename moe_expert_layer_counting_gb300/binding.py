@@ -39,8 +39,10 @@ MOE_ERR_DEVICE_INDEX = 7
 
 LAYOUT_CANONICAL, LAYOUT_MMA_L1, LAYOUT_MMA_L2 = 0, 1, 2
 PHASE_TOKEN_SCALES, PHASE_GEMM1, PHASE_GEMM2, PHASE_H_SCALES = 1, 2, 4, 8
+ROUTE_SOFTMAX, ROUTE_SIGMOID, ROUTE_RAW, ROUTE_NO_RENORM = 0, 1, 2, 4
 
-EXPORTED = ["mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_permute_workspace_size",
+EXPORTED = ["mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_route_topk_ex",
+            "moe_permute_workspace_size",
             "moe_permute", "moe_permute_noalloc", "moe_expert_workspace_size", "moe_expert_forward", "moe_combine",
             "moe_workspace_size", "moe_forward", "moe_get_device_status", "moe_status_string", "moe_version"]
 
@@ -68,12 +70,14 @@ class MoeForwardArgs(ctypes.Structure):
                 ("topk_idx_out", _p), ("topk_w_out", _p),
                 ("counts_out", _p), ("offsets_out", _p), ("perm_out", _p),
                 ("tile_n", _i32),
-                ("workspace", _p), ("workspace_bytes", _sz)]
+                ("workspace", _p), ("workspace_bytes", _sz),
+                ("route_mode", _i32)]
 
 
 lib.mxq_quantize_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.mxq_quantize_weight.argtypes = [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _p]
 lib.moe_route_topk.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p]
+lib.moe_route_topk_ex.argtypes = [_p, _i64, _i32, _i32, _i32, _p, _p, _p]
 lib.moe_permute_workspace_size.argtypes = [_i64, _i32, _i32]
 lib.moe_permute_workspace_size.restype = _sz
 lib.moe_permute.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p, _p, _p, _sz, _p]
@@ -89,7 +93,8 @@ lib.moe_get_device_status.argtypes = [_p, _p, ctypes.POINTER(ctypes.c_int)]
 lib.moe_status_string.argtypes = [ctypes.c_int]
 lib.moe_status_string.restype = ctypes.c_char_p
 lib.moe_version.restype = ctypes.c_char_p
-for _name in ("mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_permute", "moe_permute_noalloc",
+for _name in ("mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_route_topk_ex", "moe_permute",
+              "moe_permute_noalloc",
               "moe_expert_forward",
               "moe_combine", "moe_forward", "moe_get_device_status"):
     getattr(lib, _name).restype = ctypes.c_int
@@ -144,9 +149,12 @@ def mxq_quantize_weight(w: torch.Tensor, layout: int, q: torch.Tensor, s: torch.
 
 
 def moe_route_topk(logits: torch.Tensor, k: int, topk_idx: torch.Tensor, topk_w: torch.Tensor, stream=None,
-                   check=True) -> int:
+                   check=True, mode: int = ROUTE_SOFTMAX) -> int:
     T, E = logits.shape
-    rc = lib.moe_route_topk(_ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+    if mode == ROUTE_SOFTMAX:
+        rc = lib.moe_route_topk(_ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+    else:
+        rc = lib.moe_route_topk_ex(_ptr(logits), T, E, k, mode, _ptr(topk_idx), _ptr(topk_w), _stream(stream))
     if check:
         _check(rc, "moe_route_topk")
     return rc
@@ -213,14 +221,16 @@ def moe_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
 
 
 def moe_forward(x, logits, w1q, w1s, w2q, w2s, k: int, y, workspace, topk_idx_out=None, topk_w_out=None,
-                counts_out=None, offsets_out=None, perm_out=None, tile_n: int = 0, stream=None, check=True) -> int:
+                counts_out=None, offsets_out=None, perm_out=None, tile_n: int = 0, stream=None, check=True,
+                route_mode: int = ROUTE_SOFTMAX) -> int:
     T, H = x.shape
     E = logits.shape[1]
     I = w2q.shape[2] * 2
     a = MoeForwardArgs(ctypes.sizeof(MoeForwardArgs), T, H, I, E, k,
                        _ptr(x), _ptr(logits), _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s), _ptr(y),
                        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), _ptr(offsets_out),
-                       _ptr(perm_out), tile_n, _ptr(workspace), workspace.numel() * workspace.element_size())
+                       _ptr(perm_out), tile_n, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                       route_mode)
     rc = lib.moe_forward(ctypes.byref(a), _stream(stream))
     if check:
         _check(rc, "moe_forward")

@@ -105,6 +105,7 @@ extern "C" size_t moe_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E,
 extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   if (!a || a->struct_size != sizeof(moe_forward_args)) return MOE_ERR_INVALID_ARG;
   if (a->T < 0 || a->H <= 0 || a->I <= 0 || a->E <= 0 || a->k <= 0) return MOE_ERR_INVALID_ARG;
+  if (!route_mode_valid(a->route_mode)) return MOE_ERR_INVALID_ARG;
   if (!a->workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(a->workspace, 256)) return MOE_ERR_MISALIGNED;
   const ForwardWs lay = forward_ws_layout(a->T, a->H, a->I, a->E, a->k);
@@ -149,14 +150,14 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   int32_t *inv_perm = reinterpret_cast<int32_t *>(ws + lay.inv_perm);
   if (front_eligible(a->T, a->H, a->E, a->k)) {
     // small problems: routing + permute + pool cast in one launch
-    rc = launch_front(&ea, a->x, a->logits, idx, wts, inv_perm, ws + lay.expert, st);
+    rc = launch_front(&ea, a->x, a->logits, a->route_mode, idx, wts, inv_perm, ws + lay.expert, st);
     if (rc != MOE_OK) return rc;
     ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
     rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
     if (rc != MOE_OK) return rc;
     return launch_combine(ea.y_pairs, idx, a->T, a->k, a->H, a->y, st);
   }
-  rc = launch_route(a->logits, a->T, a->E, a->k, idx, wts, st);
+  rc = launch_route(a->logits, a->T, a->E, a->k, a->route_mode, idx, wts, st);
   if (rc != MOE_OK) return rc;
   rc = launch_permute(idx, a->T, a->E, a->k, counts, offsets, perm, inv_perm, status, ws + lay.perm_scratch, st);
   if (rc != MOE_OK) return rc;

@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts_out,
     int32_t *__restrict__ offsets_out, int32_t *__restrict__ perm_out, int32_t *__restrict__ inv_perm_out,
     uint8_t *__restrict__ chunks, int32_t *__restrict__ tok_pool, float *__restrict__ w_pool,
-    uint2 *__restrict__ xq_pool, int gpc) {
+    uint2 *__restrict__ xq_pool, int gpc, int mode) {
   constexpr int kW = kFrontThreads / 32;
   extern __shared__ __align__(16) unsigned char fsm[];
   const int P = T * k;
@@ -714,7 +714,7 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
   for (int t = warp; t < T; t += kW) {
     int my_idx;
     float my_w;
-    warp_route_token<kFrontMaxE / 32>(logits + (size_t)t * E, E, k, lane, &my_idx, &my_w);
+    warp_route_token<kFrontMaxE / 32>(logits + (size_t)t * E, E, k, lane, mode, &my_idx, &my_w);
     if (lane < k) {
       idx_sm[t * k + lane] = my_idx;
       w_sm[t * k + lane] = my_w;
@@ -792,8 +792,8 @@ size_t front_smem(int T, int E, int k, int gpc) {
 }
 
 template <int BN>
-int launch_front_t(const moe_expert_args *a, const uint16_t *x, const float *logits, int32_t *idx, float *wts,
-                   int32_t *inv_perm, char *ws, const ExpertWs &lay, cudaStream_t st) {
+int launch_front_t(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
+                   float *wts, int32_t *inv_perm, char *ws, const ExpertWs &lay, cudaStream_t st) {
   // one CTA per 32-value column group of the pool rows, at most two per SM
   const int groups = (int)(a->H / 32);
   const int cap = num_sms() * 2;
@@ -804,7 +804,7 @@ int launch_front_t(const moe_expert_args *a, const uint16_t *x, const float *log
                     const_cast<int32_t *>(a->counts), const_cast<int32_t *>(a->offsets),
                     const_cast<int32_t *>(a->perm), inv_perm, reinterpret_cast<uint8_t *>(ws + lay.sfb1),
                     reinterpret_cast<int32_t *>(ws + lay.tok_pool), reinterpret_cast<float *>(ws + lay.w_pool),
-                    reinterpret_cast<uint2 *>(ws + lay.xq_pool), gpc);
+                    reinterpret_cast<uint2 *>(ws + lay.xq_pool), gpc, mode);
 }
 
 template <int BN>
@@ -942,17 +942,17 @@ bool front_eligible(int64_t T, int64_t H, int E, int k) {
   return T >= 1 && T <= kFrontMaxT && E <= kFrontMaxE && T * k * H <= (int64_t(4) << 20);
 }
 
-int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int32_t *idx, float *wts,
-                 int32_t *inv_perm, void *scratch, cudaStream_t st) {
+int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
+                 float *wts, int32_t *inv_perm, void *scratch, cudaStream_t st) {
   const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
   char *ws = reinterpret_cast<char *>(scratch);
   const int bn = a->tile_n ? a->tile_n : choose_tile_n(a->T * a->k, a->E);
   switch (bn) {
-    case 16: return launch_front_t<16>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
-    case 32: return launch_front_t<32>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
-    case 64: return launch_front_t<64>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
-    case 128: return launch_front_t<128>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
-    case 224: return launch_front_t<224>(a, x, logits, idx, wts, inv_perm, ws, lay, st);
+    case 16: return launch_front_t<16>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
+    case 32: return launch_front_t<32>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
+    case 64: return launch_front_t<64>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
+    case 128: return launch_front_t<128>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
+    case 224: return launch_front_t<224>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
 }

@@ -104,7 +104,8 @@ inline int choose_tile_n(int64_t P, int64_t E) {
 // Internal launchers (return a moe_status).  `status` points at the two
 // status words of the caller's workspace.
 int launch_quant_act(const uint16_t *x, int64_t rows, int64_t K, uint8_t *q, uint8_t *s, cudaStream_t st);
-int launch_route(const float *logits, int64_t T, int E, int k, int32_t *idx, float *w, cudaStream_t st);
+int launch_route(const float *logits, int64_t T, int E, int k, int mode, int32_t *idx, float *w, cudaStream_t st);
+bool route_mode_valid(int mode);
 size_t permute_scratch_bytes(int64_t T, int E, int k);
 int launch_permute(const int32_t *idx, int64_t T, int E, int k, int32_t *counts, int32_t *offsets,
                    int32_t *perm, int32_t *inv_perm, int *status, void *scratch, cudaStream_t st);
@@ -117,8 +118,8 @@ int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch,
 // cast in one launch.  `a` supplies shapes, tile size and the counts / offsets /
 // perm outputs.
 bool front_eligible(int64_t T, int64_t H, int E, int k);
-int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int32_t *idx, float *wts,
-                 int32_t *inv_perm, void *scratch, cudaStream_t st);
+int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
+                 float *wts, int32_t *inv_perm, void *scratch, cudaStream_t st);
 int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k, int64_t H, uint16_t *y,
                    cudaStream_t st);
 

@@ -18,23 +18,48 @@ __device__ __forceinline__ float route_key_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
-// Softmax top-k routing of one token by one warp (MonoMoe kernel -- design,
-// section 1), straight from the token's E logits in global memory.
-// Selection ranks the raw logits, equal logits go to the lower expert index,
-// output in descending order; w_j = exp(l_j - l_max) / sum over the k chosen.
+// Routing modes (the ABI's MOE_ROUTE_* values): bits 0-1 the score
+// (0 softmax, 1 sigmoid, 2 raw logits), bit 2 no renormalisation (raw scores
+// are never renormalised).
+enum : int { kRouteSoftmax = 0, kRouteSigmoid = 1, kRouteRaw = 2, kRouteNoRenorm = 4 };
+
+// Top-k routing of one token by one warp (MonoMoe kernel -- design,
+// section 1: softmax or sigmoid top-K with optional renormalisation; raw
+// scores as in the MegaMoE test's topk of randn scores), straight from the
+// token's E logits in global memory.  Selection ranks the raw logits (every
+// score is an increasing function of them), equal logits go to the lower
+// expert index, output in descending order.  Weights (l_max the top logit,
+// S the k chosen):
+//   softmax:   exp(l_j - l_max) / sum over S (renormalised) or over all E
+//   sigmoid:   s_j = 1 / (1 + exp(-l_j)), divided by sum over S if renormalised
+//   raw:       l_j
 // Lane l holds the keys of experts l + 32 u (u < NV) in registers; each of
 // the k rounds takes every lane's best remaining key, the warp maximum of
 // those (redux) and, among the lanes that hold it, the lowest expert index
 // (redux again); the owner clears that key.  Lane j < k returns the j-th
 // choice in *idx_out / *w_out.  E <= 32 * NV; k <= min(E, 32).
 template <int NV>
-__device__ __forceinline__ void warp_route_token(const float *__restrict__ src, int E, int k, int lane,
+__device__ __forceinline__ void warp_route_token(const float *__restrict__ src, int E, int k, int lane, int mode,
                                                  int *idx_out, float *w_out) {
   uint32_t key[NV];
 #pragma unroll
   for (int u = 0; u < NV; ++u) {
     const int e = lane + 32 * u;
     key[u] = e < E ? route_key(__ldg(src + e)) : 0u;    // 0: no expert (below every finite logit's key)
+  }
+  const int scoring = mode & 3;
+  const bool renorm = scoring != kRouteRaw && !(mode & kRouteNoRenorm);
+  float full_sum = 0.f;                      // softmax without renormalisation: sum over all E
+  if (scoring == kRouteSoftmax && !renorm) {
+    uint32_t lk = 0;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) lk = key[u] > lk ? key[u] : lk;
+    const float lmax = route_key_value(__reduce_max_sync(0xffffffffu, lk));
+#pragma unroll
+    for (int u = 0; u < NV; ++u)
+      if (key[u] != 0u) full_sum += expf(route_key_value(key[u]) - lmax);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) full_sum += __shfl_xor_sync(0xffffffffu, full_sum, o);
   }
   int my_idx = 0;
   uint32_t my_key = 0;
@@ -52,13 +77,24 @@ __device__ __forceinline__ void warp_route_token(const float *__restrict__ src, 
       if (lane == (e & 31) && u == (e >> 5)) key[u] = 0;
   }
   const float my_val = route_key_value(my_key);
-  const float lmax = __shfl_sync(0xffffffffu, my_val, 0);
-  const float ex = lane < k ? expf(my_val - lmax) : 0.f;
-  float sum = ex;
+  float score;                               // this lane's unnormalised weight (0 for lanes >= k)
+  if (scoring == kRouteSoftmax) {
+    const float lmax = __shfl_sync(0xffffffffu, my_val, 0);
+    score = lane < k ? expf(my_val - lmax) : 0.f;
+  } else if (scoring == kRouteSigmoid) {
+    score = lane < k ? __fdiv_rn(1.f, 1.f + expf(-my_val)) : 0.f;
+  } else {
+    score = lane < k ? __ldg(src + my_idx) : 0.f;          // the logit itself (keeps the sign of a zero)
+  }
+  float denom = full_sum;
+  if (renorm) {
+    denom = score;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = 16; o > 0; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
+  }
   *idx_out = my_idx;
-  *w_out = lane < k ? __fdiv_rn(ex, sum) : 0.f;
+  *w_out = lane >= k ? 0.f : (scoring == kRouteRaw || (scoring == kRouteSigmoid && !renorm)) ? score
+                                                                                             : __fdiv_rn(score, denom);
 }
 
 // Exclusive prefix of ceil(cnt[e] / bn) over e < E into tile_off[0..E] (the

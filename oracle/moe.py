@@ -248,11 +248,12 @@ def combine(y_pairs: np.ndarray, topk_idx: np.ndarray) -> np.ndarray:
     return F.f64_to_bf16_bits(s)
 
 
-def forward(x_bf16_bits, logits_f32, w1q, w1s, w2q, w2s, k: int):
+def forward(x_bf16_bits, logits_f32, w1q, w1s, w2q, w2s, k: int, scoring: str = "softmax",
+            renormalize: bool = True):
     """The whole layer: returns dict with every intermediate and y (BF16 bits [T, H])."""
     E = w1q.shape[0]
     xq, xs = quantize_act(x_bf16_bits)
-    idx, w = route_topk(logits_f32, k)
+    idx, w = route_topk(logits_f32, k, scoring, renormalize)
     counts, offsets, perm, inv_perm = permute(idx, E)
     y_pairs, hq, hs = expert_forward(xq, xs, w1q, w1s, w2q, w2s, idx, w, E, return_h=True)
     y = combine(y_pairs, idx)

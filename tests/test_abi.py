@@ -64,6 +64,10 @@ def test_host_validation_rejects_bad_arguments():
     assert L.moe_route_topk(p, 4, 8, 9, p, p, s0) == B.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_route_topk(p, 4, 2048, 2, p, p, s0) == B.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_route_topk(p, 0, 8, 2, p, p, s0) == B.MOE_OK
+    for bad_mode in (3, 7, 8, -1):
+        assert L.moe_route_topk_ex(p, 4, 8, 2, bad_mode, p, p, s0) == B.MOE_ERR_INVALID_ARG
+    for mode in (B.ROUTE_SIGMOID, B.ROUTE_RAW, B.ROUTE_SOFTMAX | B.ROUTE_NO_RENORM, B.ROUTE_RAW | B.ROUTE_NO_RENORM):
+        assert L.moe_route_topk_ex(p, 0, 8, 2, mode, p, p, s0) == B.MOE_OK
     ws_small = 16
     assert L.moe_permute(p, 4, 8, 2, p, p, p, p, p, ws_small, s0) == B.MOE_ERR_WORKSPACE_TOO_SMALL
     assert L.moe_permute(p, 4, 8, 2, p, p, p, p, ctypes.c_void_p(0x1010), 1 << 20, s0) == B.MOE_ERR_MISALIGNED

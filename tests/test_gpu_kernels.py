@@ -204,3 +204,39 @@ def test_combine(B, T, k, H):
     ulp = np.abs(rv) * 2.0 ** -7 + 1e-38
     assert np.all(np.abs(gv - rv) <= ulp)
     assert np.mean(got != y_ref) <= 1e-3
+
+
+# ---------------------------------------------------------------- routing variants
+_MODES = {"softmax_full": ("softmax", False), "sigmoid": ("sigmoid", True),
+          "sigmoid_raw_scores": ("sigmoid", False), "raw": ("raw", False)}
+
+
+def _mode_code(B, scoring, renorm):
+    code = {"softmax": B.ROUTE_SOFTMAX, "sigmoid": B.ROUTE_SIGMOID, "raw": B.ROUTE_RAW}[scoring]
+    return code | (0 if renorm else B.ROUTE_NO_RENORM)
+
+
+@pytest.mark.parametrize("mode", list(_MODES))
+@pytest.mark.parametrize("case", _route_cases(), ids=lambda c: c[0])
+def test_route_topk_modes(B, case, mode):
+    """Selection bit-exact in every mode.  Weights: raw bit-exact; sigmoid
+    without renormalisation: expf (<= 2 ulp) scaled by e/(1+e) <= 1, one add
+    and one divide: <= 4 ulp; sigmoid renormalised: plus a k-term sum and a
+    divide: <= 8 + k ulp; softmax over all E: expf of a rounded difference
+    (<= 2 ulp + |d| * 2^-24 with |d| < 32 here), an E-term sum
+    (<= (E/32 + 5) * 2^-24 relative), a divide: <= 40 + E/32 ulp."""
+    _, logits, k = case
+    scoring, renorm = _MODES[mode]
+    T, E = logits.shape
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    B.moe_route_topk(logits.contiguous().cuda(), k, idx, w, mode=_mode_code(B, scoring, renorm))
+    idx_ref, w_ref = O.route_topk(logits.numpy(), k, scoring, renorm)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    wg = w.cpu().numpy()
+    if scoring == "raw":
+        assert np.array_equal(wg.view(np.uint32), w_ref.view(np.uint32))
+        return
+    bound = {"sigmoid": (8 + k) if renorm else 4, "softmax": 40 + E / 32}[scoring]
+    ulp = np.spacing(np.abs(w_ref).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(wg.astype(np.float64) - w_ref) <= bound * ulp + 1e-30)

@@ -47,3 +47,26 @@ def test_forward_shape(B, name):
     Hp.assert_bf16_close(y_g, ref["y"], what=name)
     if k == 1:
         assert np.all(st.w_ref == 1.0)
+
+
+@pytest.mark.parametrize("name,scoring,renorm", [("tiny", "sigmoid", True), ("small_decode", "sigmoid", False),
+                                                 ("small_decode", "softmax", False), ("tiny", "raw", False)])
+def test_forward_routing_modes(B, name, scoring, renorm):
+    """The whole layer with each routing mode (small-problem kernel), in full
+    against the oracle with the same mode."""
+    wl = W.WORKLOADS[name]
+    st = Setup(B, wl)
+    st.idx_ref, st.w_ref = O.route_topk(st.logits.numpy(), wl.k, scoring, renorm)
+    code = {"softmax": B.ROUTE_SOFTMAX, "sigmoid": B.ROUTE_SIGMOID, "raw": B.ROUTE_RAW}[scoring]
+    mode = code | (0 if renorm else B.ROUTE_NO_RENORM)
+    y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device="cuda")
+    ws = torch.empty(B.moe_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.k), dtype=torch.uint8, device="cuda")
+    B.moe_forward(st.x.cuda(), st.logits.cuda(), st.qe.w1q, st.qe.w1s, st.qe.w2q, st.qe.w2s, wl.k, y, ws,
+                  topk_idx_out=idx, route_mode=mode)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ws) == 0
+    assert np.array_equal(idx.cpu().numpy(), st.idx_ref)
+    ref = O.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, wl.k,
+                    scoring=scoring, renormalize=renorm)
+    Hp.assert_bf16_close(Hp.bits16(y), ref["y"], what=f"{name} {scoring} renorm={renorm}")
