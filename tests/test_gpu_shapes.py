@@ -70,3 +70,42 @@ def test_forward_routing_modes(B, name, scoring, renorm):
     ref = O.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, wl.k,
                     scoring=scoring, renormalize=renorm)
     Hp.assert_bf16_close(Hp.bits16(y), ref["y"], what=f"{name} {scoring} renorm={renorm}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_decode"])
+def test_dropped_pairs_end_to_end(B, name):
+    """Pairs marked dropped (index < 0, as the MegaMoE dispatch skips them)
+    through the separate entry points: permute (not counted, inv_perm -1),
+    the expert GEMMs (never see them) and the combine (skips them); y in full
+    against the oracle on the same indices."""
+    wl = W.WORKLOADS[name]
+    st = Setup(B, wl)
+    rng = np.random.default_rng(wl.seed + 99)
+    idx = st.idx_ref.copy()
+    idx[rng.random(idx.shape) < 0.25] = -1
+    w = st.w_ref
+    dev = "cuda"
+    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
+    idx_d, w_d = torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
+    inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pws = torch.empty(B.moe_permute_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
+    B.moe_permute(idx_d, E, counts, offsets, perm, inv, pws)
+    c_ref, o_ref, p_ref, i_ref = O.permute(idx, E)
+    torch.cuda.synchronize()
+    assert np.array_equal(counts.cpu().numpy(), c_ref) and np.array_equal(offsets.cpu().numpy(), o_ref)
+    n = int(o_ref[-1])
+    assert np.array_equal(perm.cpu().numpy()[:n], p_ref[:n]) and np.array_equal(inv.cpu().numpy(), i_ref)
+    xq, xs = torch.from_numpy(st.xq_ref).to(dev), torch.from_numpy(st.xs_ref).to(dev)
+    y_pairs = torch.zeros(k, T, H, dtype=torch.bfloat16, device=dev)
+    ews = torch.empty(B.moe_expert_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    B.moe_expert_forward(xq, xs, st.qe.w1q, st.qe.w1s, st.qe.w2q, st.qe.w2s, idx_d, w_d, counts, offsets, perm,
+                         y_pairs, ews)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    B.moe_combine(y_pairs, idx_d, y)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ews) == 0
+    yp_ref = O.expert_forward(st.xq_ref, st.xs_ref, st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, idx, w, E)
+    Hp.assert_bf16_close(Hp.bits16(y), O.combine(yp_ref, idx), what=f"{name} with dropped pairs")
