@@ -443,7 +443,10 @@ def launches_per_forward(T, H, E, k):
     P = T * k
     permute = 1 if P <= 2048 else 2            # single-block permute, or count + scatter
     if 1 <= T <= 64 and E <= 256 and P * H <= (4 << 20):
-        return 4                               # front (route + permute + pool cast), GEMM1, GEMM2, combine
+        ne = min(E, P)
+        if -(-P // ne) <= 16:                  # 16-token tiles
+            return 2                           # front (route + permute + pool cast), GEMM1 + GEMM2 + combine
+        return 4                               # front, GEMM1, GEMM2, combine
     if P * H <= (16 << 20):
         return 1 + permute + 1 + 3             # route, permute, pool cast, GEMM1, GEMM2, combine
     return 1 + 1 + permute + 1 + 3             # quant, route, permute, pool prep, GEMM1, GEMM2, combine

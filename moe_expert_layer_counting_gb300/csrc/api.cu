@@ -69,6 +69,7 @@ namespace {
 constexpr int64_t kPoolCastMaxValues = int64_t(16) << 20;
 
 struct ForwardWs {
+  size_t sync_end;   // status words, then the single-launch layer's arrival counters (zeroed per call)
   size_t xq, xs, idx, w, counts, offsets, perm, inv_perm, perm_scratch, expert, y_pairs, total;
 };
 
@@ -76,6 +77,8 @@ ForwardWs forward_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   const int64_t P = T * k;
   ForwardWs w;
   size_t off = kStatusBytes;
+  off += round_up(fused_sync_ints(T, (int)E, (int)k) * 4, 256);
+  w.sync_end = off;
   w.xq = off;           off += round_up((size_t)T * H, 256);
   w.xs = off;           off += round_up((size_t)T * (H / 32), 256);
   w.idx = off;          off += round_up((size_t)P * 4, 256);
@@ -138,7 +141,7 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
       return MOE_ERR_MISALIGNED;
   }
 
-  if (cudaMemsetAsync(ws, 0, 32, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (a->T == 0) {
     if (a->counts_out && cudaMemsetAsync(a->counts_out, 0, (size_t)a->E * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (a->offsets_out && cudaMemsetAsync(a->offsets_out, 0, (size_t)(a->E + 1) * 4, st) != cudaSuccess)
@@ -152,6 +155,9 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
     // small problems: routing + permute + pool cast in one launch
     rc = launch_front(&ea, a->x, a->logits, a->route_mode, idx, wts, inv_perm, ws + lay.expert, st);
     if (rc != MOE_OK) return rc;
+    // then, with 16-token tiles, both GEMMs and the combine in one more
+    if (fused_eligible(a->T, a->H, a->E, a->k, ea.tile_n))
+      return launch_fused_gemms(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
     ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
     rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
     if (rc != MOE_OK) return rc;

@@ -87,10 +87,6 @@ struct Cfg {
   static constexpr int kTmemCols = kAccBufs * BN + kSfSlot * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                          : kTmemCols <= 256 ? 256 : 512;
-  // decode-sized tiles: the weights of the next kPrefetchItems work items of
-  // a CTA are requested into L2 ahead of their TMA loads (a few bulk
-  // prefetches per work item: its tiles are contiguous in HBM)
-  static constexpr int kDefaultPrefetchItems = 0;
   // shared memory carve-up (offsets from a 1024-aligned base)
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -117,18 +113,15 @@ size_t smem_bytes(int E) {
 struct GemmArgs {
   int E, k, T, H, I;
   int M, K, KB, MT;                 // weight rows / reduction / K blocks / weight tiles per expert
-  int prefetch_items;               // L2 prefetch distance of weight tiles, in work items (0 = off)
   int inject_wait;                  // debug: 1 = the MMA warp first waits on a barrier nothing completes
   // GEMM2 launched right after GEMM1 in the same call: the expert table and
   // the first stages' weight loads are issued before griddepcontrol.wait
   // (GEMM1 signals its dependents only after its own wait, so the routing
   // outputs are final by then; weights are never written by a kernel)
   int early_weights;
-  uint32_t prefetch_bytes;          // bytes of codes prefetched per work item
   const int32_t *counts, *offsets, *perm;
   const int32_t *tok_pool;          // token of each pool row (GEMM1 gather)
   const float *w_pool;              // top-k weight of each pool row (GEMM1 epilogue)
-  const uint8_t *w_codes;           // weight codes, tile-contiguous (L2 prefetch)
   const uint8_t *w_sf;              // [E][MT][KB][512]
   const uint8_t *b_sf;              // [tiles][KB][512]
   uint8_t *hq;                      // L1 out [P][I] (pool order)
@@ -136,6 +129,13 @@ struct GemmArgs {
   uint8_t *hs_out;                  // optional L1 out [P][I/32]
   uint16_t *y_pairs;                // L2 out [k][T][H]
   int *status;
+  // GEMM1 + GEMM2 + combine in one launch (PHASE 3): GEMM2's operands, the
+  // arrival counters and the combine
+  int MT2, KB2;
+  const uint8_t *w_sf2, *b_sf2;
+  int *sync;                        // [0] GEMM2 items done, [1 + g] GEMM1 items of token tile g done
+  const int32_t *topk_idx;          // [T][k] (combine: dropped slots skipped)
+  uint4 *y;                         // [T][H] bf16 (combine output)
 };
 
 struct TileInfo {
@@ -200,8 +200,13 @@ __device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int 
 template <int BN, int PHASE>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
+                       const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_b2,
                        const GemmArgs args) {
+  // PHASE 1: GEMM1 + SwiGLU epilogue; 2: GEMM2; 3: both and the combine in
+  // one launch (small problems): GEMM1 items, then GEMM2 items (each waiting
+  // on the GEMM1 items of its token tile), then the combine
   using C = Cfg<BN>;
+  constexpr bool kFused = PHASE == 3;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
@@ -219,6 +224,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
   int *off_sm = cnt_sm + (args.E + 1);
   int32_t *row_pair_buf = reinterpret_cast<int32_t *>(smem + C::kOffRow);
   float *row_w_buf = reinterpret_cast<float *>(smem + C::kOffRow + 8 * BN);
+  int *scan_ws = reinterpret_cast<int *>(smem + C::kOffScan);            // block-scan scratch
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int *status = args.status;
@@ -233,6 +239,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
       tma_prefetch_desc(&tmap_b);
+      if (kFused) {
+        tma_prefetch_desc(&tmap_w2);
+        tma_prefetch_desc(&tmap_b2);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -261,13 +271,30 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
   if (PHASE == 1) pdl_launch_dependents();
   load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm, early);
   __syncthreads();
-  block_tile_map<C::kThreads>(cnt_sm, args.E, BN, tile_off, reinterpret_cast<int *>(smem + C::kOffScan),
-                              reinterpret_cast<int *>(smem + C::kOffScan) + 15);
+  block_tile_map<C::kThreads>(cnt_sm, args.E, BN, tile_off, scan_ws, scan_ws + 15);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_ptr;
-  const int total_work = tile_off[args.E] * args.MT;
+  const int n1 = tile_off[args.E] * args.MT;                     // GEMM1 items (PHASE 3: then GEMM2's)
+  const int n2 = kFused ? tile_off[args.E] * args.MT2 : 0;
+  const int total_work = n1 + n2;
+  // work item w: its tile, weight tiles per expert, K blocks, and whether it
+  // is a GEMM1 item
+  struct Item {
+    TileInfo ti;
+    int MT, KB;
+    bool l1;
+  };
+  auto get_item = [&](int w) {
+    Item it;
+    it.l1 = PHASE == 1 || (kFused && w < n1);
+    const bool second = kFused && !it.l1;
+    it.MT = second ? args.MT2 : args.MT;
+    it.KB = second ? args.KB2 : args.KB;
+    it.ti = decode_work<BN>(second ? w - n1 : w, it.MT, args.E, tile_off, cnt_sm, off_sm);
+    return it;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -275,72 +302,122 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;
     bool ok = true;
-    // L2 prefetch of whole work items (codes and scales of all K blocks),
-    // kept prefetch_items items ahead of the item being loaded.
-    const int pf_items = args.prefetch_items;
-    auto prefetch_item = [&](int w) {
-      if (w >= total_work || lane != 0) return;
-      const TileInfo t = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
-      const size_t first = (size_t)(t.e * args.MT + t.mt) * args.KB;
-      const uint8_t *codes = args.w_codes + first * kWTileBytes;
-      const uint32_t code_bytes = min((uint32_t)args.KB * kWTileBytes, args.prefetch_bytes);
-      for (uint32_t off = 0; off < code_bytes; off += 65536u)
-        prefetch_l2_bulk(codes + off, min(65536u, code_bytes - off));
-      prefetch_l2_bulk(args.w_sf + first * 512, (uint32_t)args.KB * 512);
-    };
-    for (int i = 0; i <= pf_items && pf_items > 0; ++i) prefetch_item(blockIdx.x + i * gridDim.x);
     // one stage = the weight part (codes + weight scales, static data) and the
-    // token part (pool rows or h, token scales, written by earlier kernels);
-    // the stage's barrier expects both
-    auto issue_weights = [&](int st, int kb, int nk, int wtile) {
+    // token part (pool rows or h, token scales, written by earlier kernels or,
+    // in PHASE 3, by other CTAs); the stage's barrier expects both
+    auto issue_weights = [&](int st, int kb, int nk, int wtile, const Item &it) {
+      const bool second = kFused && !it.l1;
       const uint32_t sfb_bytes = (uint32_t)((nk - 1) * C::kTokChunk + C::kSfbBytes);
       // the weight box always spans kKBS tiles (rows past the tensor read as zeros);
       // the FP4-unpacking load completes the packed byte count
       mbar_arrive_expect_tx(&full[st], (uint32_t)(C::kKBS * kWTileBytes + nk * C::kBTile + nk * 512) + sfb_bytes);
-      tma_load_2d(smem + C::kOffA + st * C::kABytes, &tmap_w, &full[st], 0, (wtile + kb) * kBM);
-      bulk_load(smem + C::kOffSfa + st * C::kKBS * 512, args.w_sf + ((size_t)wtile + kb) * 512, nk * 512, &full[st]);
+      tma_load_2d(smem + C::kOffA + st * C::kABytes, second ? &tmap_w2 : &tmap_w, &full[st], 0,
+                  (wtile + kb) * kBM);
+      bulk_load(smem + C::kOffSfa + st * C::kKBS * 512, (second ? args.w_sf2 : args.w_sf) + ((size_t)wtile + kb) * 512,
+                nk * 512, &full[st]);
     };
-    auto issue_tokens = [&](int st, int kb, int nk, const TileInfo &ti) {
+    auto issue_tokens = [&](int st, int kb, int nk, const Item &it) {
+      const bool second = kFused && !it.l1;
       const uint32_t sfb_bytes = (uint32_t)((nk - 1) * C::kTokChunk + C::kSfbBytes);
-      const uint8_t *sfb_src = args.b_sf + ((size_t)ti.g * args.KB + kb) * C::kTokChunk;
+      const uint8_t *sfb_src = (second ? args.b_sf2 : args.b_sf) + ((size_t)it.ti.g * it.KB + kb) * C::kTokChunk;
       bulk_load(smem + C::kOffSfb + st * C::kKBS * C::kTokChunk, sfb_src, sfb_bytes, &full[st]);
       unsigned char *b_dst = smem + C::kOffB + st * C::kBBytes;
-      for (int i = 0; i < nk; ++i) tma_load_2d(b_dst + i * C::kBTile, &tmap_b, &full[st], (kb + i) * kBK, ti.s0);
+      for (int i = 0; i < nk; ++i)
+        tma_load_2d(b_dst + i * C::kBTile, second ? &tmap_b2 : &tmap_b, &full[st], (kb + i) * kBK, it.ti.s0);
     };
-    // early_weights: the first item's first stages get their weight part now,
-    // their token part after griddepcontrol.wait (all stages are free here)
-    int pre = 0;
-    if (early) {
-      if (blockIdx.x < total_work) {
-        const TileInfo t0 = decode_work<BN>(blockIdx.x, args.MT, args.E, tile_off, cnt_sm, off_sm);
-        const int wtile0 = (t0.e * args.MT + t0.mt) * args.KB;
-        for (; pre < C::kStages && pre * C::kKBS < args.KB; ++pre)
-          if (lane == 0) issue_weights(pre, pre * C::kKBS, min(C::kKBS, args.KB - pre * C::kKBS), wtile0);
+    auto advance = [&]() {
+      issued_mask |= 1u << stage;
+      issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+      if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+    };
+    if (kFused) {
+      // every GEMM2 item: the weight part of its first stages, then the wait
+      // for the h rows of its token tile (the GEMM1 items of every weight
+      // tile of that expert), then the token parts; the token parts are issued
+      // even after a failed wait so that every armed barrier completes (the
+      // status word says why).  GEMM1 items depend on nothing in the launch.
+      for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+        const Item it = get_item(w);
+        const int wtile = (it.ti.e * it.MT + it.ti.mt) * it.KB;
+        const int nst = (it.KB + C::kKBS - 1) / C::kKBS;
+        const int npre = min(nst, C::kStages);
+        const int st0 = stage;
+        const uint32_t ph0 = phase;
+        int armed = 0;
+        for (; armed < npre; ++armed) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty,
+                                                 armed * C::kKBS)))
+            break;
+          if (lane == 0) issue_weights(stage, armed * C::kKBS, min(C::kKBS, it.KB - armed * C::kKBS), wtile, it);
+          __syncwarp();
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
+        bool dep_ok = true;
+        if (lane == 0 && !it.l1) {
+          dep_ok = wait_counter(args.sync + 1 + it.ti.g, args.MT, status, kWaitLimit, w);
+          fence_proxy_async_global();
+        }
+        dep_ok = __shfl_sync(0xffffffffu, dep_ok ? 1 : 0, 0) != 0;
+        for (int a = 0; a < armed; ++a) {
+          // armed <= kStages: the ring wraps at most once inside one item
+          const int st = (st0 + a) % C::kStages;
+          const uint32_t ph = ph0 ^ (uint32_t)((st0 + a) / C::kStages);
+          if (lane == 0) issue_tokens(st, a * C::kKBS, min(C::kKBS, it.KB - a * C::kKBS), it);
+          issued_mask |= 1u << st;
+          issued_phase = (issued_phase & ~(1u << st)) | (ph << st);
+        }
         __syncwarp();
-      }
-      pdl_wait();
-    }
-    for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
-      const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
-      if (pf_items > 0 && w != (int)blockIdx.x) prefetch_item(w + pf_items * (int)gridDim.x);
-      const int wtile = (ti.e * args.MT + ti.mt) * args.KB;        // first weight tile of this item
-      for (int kb = 0; kb < args.KB; kb += C::kKBS) {
-        const int nk = min(C::kKBS, args.KB - kb);                   // K blocks in this stage
-        const bool pre_armed = w == (int)blockIdx.x && kb < pre * C::kKBS;
-        if (!pre_armed &&
-            !__all_sync(0xffffffffu,
-                        MXQ_TIMED_WAIT(0, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb)))) {
+        if (armed < npre || !dep_ok) {
           ok = false;
           break;
         }
-        if (lane == 0) {
-          if (!pre_armed) issue_weights(stage, kb, nk, wtile);
-          issue_tokens(stage, kb, nk, ti);
+        for (int a = npre; a < nst; ++a) {
+          const int kb = a * C::kKBS;
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb))) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            issue_weights(stage, kb, min(C::kKBS, it.KB - kb), wtile, it);
+            issue_tokens(stage, kb, min(C::kKBS, it.KB - kb), it);
+          }
+          __syncwarp();
+          advance();
         }
-        __syncwarp();
-        issued_mask |= 1u << stage;
-        issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+      }
+    } else {
+      // early_weights: the first item's first stages get their weight part now,
+      // their token part after griddepcontrol.wait (all stages are free here)
+      int pre = 0;
+      if (early) {
+        if (blockIdx.x < total_work) {
+          const Item it0 = get_item(blockIdx.x);
+          const int wtile0 = (it0.ti.e * it0.MT + it0.ti.mt) * it0.KB;
+          for (; pre < C::kStages && pre * C::kKBS < args.KB; ++pre)
+            if (lane == 0) issue_weights(pre, pre * C::kKBS, min(C::kKBS, args.KB - pre * C::kKBS), wtile0, it0);
+          __syncwarp();
+        }
+        pdl_wait();
+      }
+      for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
+        const Item it = get_item(w);
+        const int wtile = (it.ti.e * it.MT + it.ti.mt) * it.KB;        // first weight tile of this item
+        for (int kb = 0; kb < it.KB; kb += C::kKBS) {
+          const int nk = min(C::kKBS, it.KB - kb);                     // K blocks in this stage
+          const bool pre_armed = w == (int)blockIdx.x && kb < pre * C::kKBS;
+          if (!pre_armed &&
+              !__all_sync(0xffffffffu,
+                          MXQ_TIMED_WAIT(0, mbar_wait(&empty[stage], phase ^ 1, status, kWaitLimit, kWaitProducerEmpty, kb)))) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            if (!pre_armed) issue_weights(stage, kb, nk, wtile, it);
+            issue_tokens(stage, kb, nk, it);
+          }
+          __syncwarp();
+          advance();
+        }
       }
     }
     // never leave with copies in flight: wait for the last load of each stage
@@ -356,9 +433,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total_work && ok; w += gridDim.x) {
-      const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      const Item it = get_item(w);
       // MMA N covers the valid tokens of the tile, rounded up to 16
-      const uint32_t n_mma = (uint32_t)min(BN, (ti.valid + 15) & ~15);
+      const uint32_t n_mma = (uint32_t)min(BN, (it.ti.valid + 15) & ~15);
       if (!__all_sync(0xffffffffu,
                       MXQ_TIMED_WAIT(2, mbar_wait(&tmem_empty[acc], acc_phase ^ 1, status, kWaitLimit, kWaitMmaTmemEmpty, w))))
         break;
@@ -368,8 +445,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
         break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      for (int kb = 0; kb < args.KB; kb += C::kKBS) {
-        const int nk = min(C::kKBS, args.KB - kb);
+      for (int kb = 0; kb < it.KB; kb += C::kKBS) {
+        const int nk = min(C::kKBS, it.KB - kb);
         if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(1, mbar_wait(&full[stage], phase, status, kWaitLimit, kWaitMmaFull, kb)))) {
           ok = false;
           break;
@@ -424,14 +501,15 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     uint32_t acc_phase = 0;
     int rb = 0;                              // row-info buffer of this item
     for (int w = blockIdx.x; w < total_work; w += gridDim.x) {
-      const TileInfo ti = decode_work<BN>(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      const Item it = get_item(w);
+      const TileInfo &ti = it.ti;
       // a half may start this item while the other still reads the previous
       // item's row info, so items alternate between two buffers (one is
       // reused two items later, after every warp passed this item's vote)
       int32_t *row_pair = row_pair_buf + rb * BN;
       float *row_w = row_w_buf + rb * BN;
       if (et < ti.valid) {
-        if (PHASE == 1) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
+        if (it.l1) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
         else row_pair[et] = __ldg(args.perm + ti.s0 + et);
       }
       // the epilogue warps agree on the outcome of the bounded wait before any
@@ -449,7 +527,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
         uint32_t v[16];
         tmem_ld_32x32b_x16(t_row + (uint32_t)c0, v);
         tmem_ld_wait();
-        if (PHASE == 1) {
+        if (it.l1) {
           // lane l of quadrant q holds stored row 32q+l: gate when (l & 8) == 0,
           // the matching up row sits 8 lanes away (8-row gate/up interleave).
           const bool is_gate = (lane & 8) == 0;
@@ -520,6 +598,16 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
       if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1; }
       rb ^= 1;
+      if (kFused) {
+        // publish the item: GEMM1 -> its h rows and scale chunk (read by other
+        // CTAs' TMA: proxy fence), GEMM2 -> its y_pairs rows (the combine)
+        fence_proxy_async_global();
+        named_bar_sync(1, 32 * C::kEpiWarps);
+        if (et == 0) {
+          __threadfence();
+          atomicAdd(it.l1 ? args.sync + 1 + ti.g : args.sync, 1);
+        }
+      }
     }
   }
 #ifdef MOE_MXQ_WAIT_STATS
@@ -539,6 +627,48 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemAlloc);
+  }
+  if (kFused) {
+    // combine (MegaMoE notes, "Combine"): once every GEMM2 item of the launch
+    // has published its rows, each CTA sums the k BF16 rows of its share of
+    // (token, 8-value chunk) items in FP32, in slot order, and casts once
+    if (threadIdx.x == 0) scan_ws[0] = wait_counter(args.sync, n2, status, kWaitLimit, total_work) ? 1 : 0;
+    __syncthreads();
+    if (scan_ws[0]) {
+      const int H8 = args.H / 8;
+      const int items = args.T * H8;
+      const uint4 *yp = reinterpret_cast<const uint4 *>(args.y_pairs);
+      for (int i = (int)blockIdx.x * C::kThreads + (int)threadIdx.x; i < items; i += (int)gridDim.x * C::kThreads) {
+        const int t = i / H8;
+        float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j0 = 0; j0 < args.k; j0 += 8) {
+          bool use[8];
+          uint4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) use[u] = j0 + u < args.k && __ldg(args.topk_idx + t * args.k + j0 + u) >= 0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (use[u]) v[u] = __ldcg(yp + (size_t)(j0 + u) * items + i);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (!use[u]) continue;
+            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+              acc8[2 * q2] += bf16_bits_to_float(wv[q2] & 0xFFFFu);
+              acc8[2 * q2 + 1] += bf16_bits_to_float(wv[q2] >> 16);
+            }
+          }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
+          o[q2] = *reinterpret_cast<const uint32_t *>(&b2);
+        }
+        args.y[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
   }
 }
 
@@ -872,18 +1002,6 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
   const size_t sm = smem_bytes<BN>(E);
   const int grid = num_sms() * C::kCtasPerSm;
-  // L2 budget for prefetched weights: ~64 MB over the grid, one or two items ahead
-  if (const char *env = getenv("MOE_MXQ_DEBUG_INJECT_WAIT")) g.inject_wait = atoi(env);
-  const auto set_prefetch = [&](int64_t KB) {
-    const int64_t item = KB * (kWTileBytes + 512);
-    const int64_t budget = (64ll << 20) / grid;
-    int items = C::kDefaultPrefetchItems;
-    if (const char *env = getenv("MOE_MXQ_PREFETCH_ITEMS")) items = atoi(env);
-    if (items > 0) items = (int)std::max<int64_t>(1, std::min<int64_t>(items, budget / item));
-    g.prefetch_items = items;
-    g.prefetch_bytes = (uint32_t)std::min<int64_t>(KB * kWTileBytes, items > 0 ? budget / items : 0) & ~15u;
-  };
-
   if (phases & MOE_PHASE_GEMM1) {
     // GEMM1 + SwiGLU (.) weight + FP8 requantisation
     const uint64_t wrows = (uint64_t)E * (2 * a->I / 128) * (a->H / 128) * 128;
@@ -894,10 +1012,9 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
                               (uint64_t)a->H, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
     g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
-    g.w_codes = a->w1q; g.w_sf = a->w1s; g.b_sf = sfb1;
-    set_prefetch(g.KB);
+    g.w_sf = a->w1s; g.b_sf = sfb1;
     if (!set_gemm_attrs(expert_gemm_kernel<BN, 1>, sm)) return MOE_ERR_CUDA;
-    if (launch_pdl(expert_gemm_kernel<BN, 1>, dim3(grid), dim3(C::kThreads), sm, st, tw1, tb, g) != MOE_OK)
+    if (launch_pdl(expert_gemm_kernel<BN, 1>, dim3(grid), dim3(C::kThreads), sm, st, tw1, tb, tw1, tb, g) != MOE_OK)
       return MOE_ERR_CUDA;
   }
   if (phases & MOE_PHASE_GEMM2) {
@@ -910,12 +1027,11 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
                               (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
     g.M = (int)a->H; g.K = (int)a->I; g.KB = (int)(a->I / 128); g.MT = (int)(a->H / 128);
-    g.w_codes = a->w2q; g.w_sf = a->w2s; g.b_sf = sfb2;
+    g.w_sf = a->w2s; g.b_sf = sfb2;
     g.early_weights = (phases & MOE_PHASE_GEMM1) ? 1 : 0;
-    set_prefetch(g.KB);
     g.hs_out = nullptr;
     if (!set_gemm_attrs(expert_gemm_kernel<BN, 2>, sm)) return MOE_ERR_CUDA;
-    if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(grid), dim3(C::kThreads), sm, st, tw2, th, g) != MOE_OK)
+    if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(grid), dim3(C::kThreads), sm, st, tw2, th, tw2, th, g) != MOE_OK)
       return MOE_ERR_CUDA;
   }
   return MOE_OK;
@@ -955,6 +1071,66 @@ int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logit
     case 224: return launch_front_t<224>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
+}
+
+// GEMM1 + GEMM2 + combine in one launch (16-token tiles, after the
+// small-problem front kernel).  Its CTAs wait on one another's arrival
+// counters, so all of them must be resident at once: kCtasPerSm CTAs of this
+// shared-memory size have to fit on an SM.
+bool fused_eligible(int64_t T, int64_t H, int E, int k, int tile_n) {
+  if (!front_eligible(T, H, E, k)) return false;
+  if (tile_n != 0 && tile_n != 16) return false;
+  if (choose_tile_n(T * k, E) != 16) return false;
+  static int smem_per_sm = -1;
+  if (smem_per_sm < 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+      v = 0;
+    smem_per_sm = v;
+  }
+  return (int64_t)Cfg<16>::kCtasPerSm * ((int64_t)smem_bytes<16>(E) + 1024) <= smem_per_sm;
+}
+
+size_t fused_sync_ints(int64_t T, int E, int k) { return 1 + (size_t)max_token_tiles(T * k, E, 16); }
+
+int launch_fused_gemms(const moe_expert_args *a, uint16_t *y, int *sync, int *status, char *ews, cudaStream_t st) {
+  using C = Cfg<16>;
+  constexpr int BN = 16;
+  const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
+  const int64_t P = a->T * a->k;
+  const int E = a->E;
+  uint8_t *sfb1 = reinterpret_cast<uint8_t *>(ews + lay.sfb1);
+  uint8_t *sfb2 = reinterpret_cast<uint8_t *>(ews + lay.sfb2);
+  uint8_t *hq = reinterpret_cast<uint8_t *>(ews + lay.hq);
+  uint8_t *xq_pool = reinterpret_cast<uint8_t *>(ews + lay.xq_pool);
+  CUtensorMap tw1, tb, tw2, th;
+  const uint64_t wrows1 = (uint64_t)E * (2 * a->I / 128) * (a->H / 128) * 128;
+  const uint64_t wrows2 = (uint64_t)E * (a->H / 128) * (a->I / 128) * 128;
+  bool ok = encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, 128, wrows1, 64, 128,
+                           C::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)xq_pool, (uint64_t)a->H, (uint64_t)P,
+                            (uint64_t)a->H, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, 128, wrows2, 64, 128,
+                            C::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
+                            (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return MOE_ERR_CUDA;
+  GemmArgs g{};
+  g.E = E; g.k = a->k; g.T = (int)a->T; g.H = (int)a->H; g.I = (int)a->I;
+  g.M = (int)(2 * a->I); g.K = (int)a->H; g.KB = (int)(a->H / 128); g.MT = (int)(2 * a->I / 128);
+  g.MT2 = (int)(a->H / 128); g.KB2 = (int)(a->I / 128);
+  g.counts = a->counts; g.offsets = a->offsets; g.perm = a->perm;
+  g.tok_pool = reinterpret_cast<int32_t *>(ews + lay.tok_pool);
+  g.w_pool = reinterpret_cast<float *>(ews + lay.w_pool);
+  g.w_sf = a->w1s; g.b_sf = sfb1; g.w_sf2 = a->w2s; g.b_sf2 = sfb2;
+  g.hq = hq; g.sfb2 = sfb2; g.hs_out = nullptr; g.y_pairs = a->y_pairs; g.status = status;
+  g.sync = sync; g.topk_idx = a->topk_idx; g.y = reinterpret_cast<uint4 *>(y);
+  if (const char *env = getenv("MOE_MXQ_DEBUG_INJECT_WAIT")) g.inject_wait = atoi(env);
+  const size_t sm = smem_bytes<BN>(E);
+  if (!set_gemm_attrs(expert_gemm_kernel<BN, 3>, sm)) return MOE_ERR_CUDA;
+  return launch_pdl(expert_gemm_kernel<BN, 3>, dim3(num_sms() * C::kCtasPerSm), dim3(C::kThreads), sm, st, tw1, tb,
+                    tw2, th, g);
 }
 
 int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, cudaStream_t st) {

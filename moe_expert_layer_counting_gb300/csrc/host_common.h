@@ -118,6 +118,13 @@ int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch,
 // cast in one launch.  `a` supplies shapes, tile size and the counts / offsets /
 // perm outputs.
 bool front_eligible(int64_t T, int64_t H, int E, int k);
+// GEMM1 + GEMM2 + combine in one launch after the front kernel (16-token
+// tiles, all CTAs co-resident): eligibility, the arrival counters it needs
+// (zeroed before the launch), and the launch (y: [T][H] output; ews: the
+// expert workspace the front kernel filled).
+bool fused_eligible(int64_t T, int64_t H, int E, int k, int tile_n);
+size_t fused_sync_ints(int64_t T, int E, int k);
+int launch_fused_gemms(const moe_expert_args *a, uint16_t *y, int *sync, int *status, char *ews, cudaStream_t st);
 int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
                  float *wts, int32_t *inv_perm, void *scratch, cudaStream_t st);
 int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k, int64_t H, uint16_t *y,

@@ -31,6 +31,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy global accesses with later async-proxy
+// (TMA) accesses: a writer runs it after stores that another CTA's TMA will
+// read, a reader after it acquired the flag that publishes them.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // A kernel launched with programmatic stream serialization may start while the
 // previous kernel of the stream is still running.  pdl_wait() blocks until
@@ -76,7 +89,8 @@ enum : int {
   kWaitEpiTmemFull = 4,
   kWaitProducerDrain = 5,
   kWaitMmaDone = 6,
-  kWaitInjected = 7       // debug: a wait on a barrier that nothing completes
+  kWaitInjected = 7,      // debug: a wait on a barrier that nothing completes
+  kWaitArrival = 8        // single-launch layer: a CTA waiting on other CTAs' arrival counter
 };
 
 // Waits for phase `parity` of `bar` to complete.  Gives up after `limit`
@@ -103,6 +117,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *w
       atomicExch(ws_status + 1, 1);
       return false;
     }
+  }
+}
+
+// Waits (bounded) until *counter >= target, the counter being raised by
+// other CTAs of the same launch (release: fence + atomic add).  Acquire load,
+// so their earlier writes are visible to this thread afterwards.  Same
+// timeout and abort protocol as mbar_wait.  One thread calls it.
+__device__ __forceinline__ bool wait_counter(const int *counter, int target, int *ws_status, long long limit,
+                                             int pos = 0) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const long long t0 = clock64();
+  volatile int *abort_flag = ws_status + 1;
+  while (true) {
+    if (ld_acquire_gpu(counter) >= target) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      if (atomicCAS(ws_status + 2, 0, kWaitArrival) == 0) {
+        ws_status[3] = (int)blockIdx.x;
+        ws_status[4] = pos;
+      }
+      report_status(ws_status, kStatusTimeout);
+      atomicExch(ws_status + 1, 1);
+      return false;
+    }
+    __nanosleep(128);
   }
 }
 
