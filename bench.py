@@ -37,17 +37,18 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM GB/s)"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
-# GEMM phase, from one-pass ncu captures (first graph replay, L2 flushed before
-# it) of the GEMM kernel built from sources whose SHA-256 is `src_sha256`
+# GEMM phase alone (the launch the roofline times), from one-pass ncu captures
+# (ncu flushes the caches before each captured launch) of the GEMM kernel
+# built from sources whose SHA-256 is `src_sha256`
 # (commands and figures in profiles/).  `traffic` is reported as null once
 # those sources change.
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC = {
-    "src_sha256": "a18ea1f6fdae4bcb0f8f10bf5703de1fda4683934e82ed4bd01158d08ac27445",
-    "small_decode": {"gemm1": 62803968 + 444416, "gemm2": 31332864 + 0},
-    "large_decode": {"gemm1": 3959629824 + 5291520, "gemm2": 1976348160 + 13918720},
-    "prefill": {"gemm1": 4245730048 + 70437888, "gemm2": 2068126208 + 451033856},
-    "skewed_prefill": {"gemm1": 3181436416 + 142319104, "gemm2": 1334934784 + 939408640},
+    "src_sha256": "b9bc33a8f1aac78d92987a8173887236e21c6a9903690671a90e400688641690",
+    "small_decode": {"gemm1": 62791680 + 12032, "gemm2": 31326464 + 0},
+    "large_decode": {"gemm1": 3959697408 + 2406912, "gemm2": 1976327680 + 13979904},
+    "prefill": {"gemm1": 4244078592 + 67489280, "gemm2": 2068602112 + 451102208},
+    "skewed_prefill": {"gemm1": 3183461888 + 139540992, "gemm2": 1335301888 + 939533824},
 }
 UNIT = "tokens/s"
 
@@ -255,33 +256,32 @@ def run_ours(args, rank, world, local_rank):
     if args.launch_list:
         timed_loop(graph.replay, args.warmup + args.steps)
         torch.cuda.synchronize()
-        return {"launch_list": True, "workload": wl.describe(), "replays": args.warmup + args.steps}
-
-    # warm-up, then a short soak so that the clock sampler sees the GPU under load
-    timed_loop(graph.replay, args.warmup)
-    if world > 1:
-        torch.distributed.barrier()
-    with ClockSampler(gpu_id_for(dev)) as clk:
-        t_soak = time.time()
-        while time.time() - t_soak < 1.5:
-            timed_loop(graph.replay, 20)
+    else:
+        # warm-up, then a short soak so that the clock sampler sees the GPU under load
+        timed_loop(graph.replay, args.warmup)
         if world > 1:
             torch.distributed.barrier()
-        torch.cuda.synchronize()
-        t0 = time.time()
-        times = timed_loop(graph.replay, args.steps)
-        torch.cuda.synchronize()
-        wall = time.time() - t0
+        with ClockSampler(gpu_id_for(dev)) as clk:
+            t_soak = time.time()
+            while time.time() - t_soak < 1.5:
+                timed_loop(graph.replay, 20)
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            t0 = time.time()
+            times = timed_loop(graph.replay, args.steps)
+            torch.cuda.synchronize()
+            wall = time.time() - t0
+            if world > 1:
+                torch.distributed.barrier()
+        assert B.moe_get_device_status(ws, stream) == 0, "device status word reports an error"
+        total_ms = sum(times)
+        mean_ms = total_ms / len(times)
         if world > 1:
-            torch.distributed.barrier()
-    assert B.moe_get_device_status(ws, stream) == 0, "device status word reports an error"
-    total_ms = sum(times)
-    mean_ms = total_ms / len(times)
-    if world > 1:
-        t = torch.tensor([total_ms, mean_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, mean_ms = float(t[0]), float(t[1])
-    value = world * T * args.steps / (total_ms / 1e3)
+            t = torch.tensor([total_ms, mean_ms], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            total_ms, mean_ms = float(t[0]), float(t[1])
+        value = world * T * args.steps / (total_ms / 1e3)
 
     # per-GEMM timing (dominant kernel) with the layer's own routing
     ews = torch.empty(B.moe_expert_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
@@ -298,6 +298,14 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         phase(B.PHASE_TOKEN_SCALES | B.PHASE_GEMM1 | B.PHASE_GEMM2)
     stream.synchronize()
+    if args.launch_list:
+        # after the forward replays: one launch of each GEMM phase alone (the
+        # kernels the roofline figures describe)
+        with torch.cuda.stream(stream):
+            phase(B.PHASE_GEMM1)
+            phase(B.PHASE_GEMM2)
+        torch.cuda.synchronize()
+        return {"launch_list": True, "workload": wl.describe(), "replays": args.warmup + args.steps}
     g1 = timed_loop(lambda: phase(B.PHASE_GEMM1), max(args.steps, 20))
     g2 = timed_loop(lambda: phase(B.PHASE_GEMM2), max(args.steps, 20))
     assert B.moe_get_device_status(ews, stream) == 0
