@@ -44,7 +44,7 @@ METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM G
 # those sources change.
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC = {
-    "src_sha256": "b9bc33a8f1aac78d92987a8173887236e21c6a9903690671a90e400688641690",
+    "src_sha256": "569750d60b7ebe9b861ead1797afac4f2febc3b1695a8c4ff1325e9a818b1711",
     "small_decode": {"gemm1": 62791680 + 12032, "gemm2": 31326464 + 0},
     "large_decode": {"gemm1": 3959697408 + 2406912, "gemm2": 1976327680 + 13979904},
     "prefill": {"gemm1": 4244078592 + 67489280, "gemm2": 2068602112 + 451102208},

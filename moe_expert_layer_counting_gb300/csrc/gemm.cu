@@ -1002,6 +1002,7 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
   const size_t sm = smem_bytes<BN>(E);
   const int grid = num_sms() * C::kCtasPerSm;
+  if (const char *env = getenv("MOE_MXQ_DEBUG_INJECT_WAIT")) g.inject_wait = atoi(env);
   if (phases & MOE_PHASE_GEMM1) {
     // GEMM1 + SwiGLU (.) weight + FP8 requantisation
     const uint64_t wrows = (uint64_t)E * (2 * a->I / 128) * (a->H / 128) * 128;

@@ -20,14 +20,14 @@ pytestmark = pytest.mark.gpu
 WAIT_SITE_INJECTED = 7
 
 
-def _tiny():
+def _tiny(tile_n=0):
     import workloads as W
     from moe_expert_layer_counting_gb300.layer import MoELayer, QuantizedExperts
     wl = W.WORKLOADS["tiny"]
     x, logits = W.tokens(wl)
     l1, l2 = W.all_expert_weights(wl, "cpu")
     qe = QuantizedExperts.from_bf16(l1.cuda(), l2.cuda())
-    return wl, x, logits, l1, l2, MoELayer(qe, wl.k, wl.T)
+    return wl, x, logits, l1, l2, MoELayer(qe, wl.k, wl.T, tile_n=tile_n)
 
 
 def _oracle_y(wl, x, logits, l1, l2):
@@ -40,13 +40,16 @@ def _oracle_y(wl, x, logits, l1, l2):
     return O.forward(bits(x), logits.numpy(), w1q, w1s, w2q, w2s, wl.k)["y"]
 
 
-def test_injected_wait_times_out_then_recovers(monkeypatch):
+@pytest.mark.parametrize("tile_n", [16, 32])
+def test_injected_wait_times_out_then_recovers(monkeypatch, tile_n):
+    """tile_n 16: GEMM1 + GEMM2 + combine in one launch (CTAs also wait on
+    one another's arrival counters); 32: separate GEMM launches."""
     from helpers import lib
     lib()
     from moe_expert_layer_counting_gb300 import binding as B
     from oracle import formats as F
 
-    wl, x, logits, l1, l2, layer = _tiny()
+    wl, x, logits, l1, l2, layer = _tiny(tile_n)
     xd, ld = x.cuda(), logits.cuda()
     layer(xd, ld)                                  # warm-up (module load, tensor maps)
     torch.cuda.synchronize()

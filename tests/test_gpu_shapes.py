@@ -109,3 +109,14 @@ def test_dropped_pairs_end_to_end(B, name):
     assert B.moe_get_device_status(ews) == 0
     yp_ref = O.expert_forward(st.xq_ref, st.xs_ref, st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, idx, w, E)
     Hp.assert_bf16_close(Hp.bits16(y), O.combine(yp_ref, idx), what=f"{name} with dropped pairs")
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 224])
+def test_forward_tiny_tile_sizes(B, tile_n):
+    """The small-problem path with every launch structure: 16-token tiles run
+    GEMM1 + GEMM2 + combine in one launch, larger tiles as separate launches."""
+    wl = W.WORKLOADS["tiny"]
+    st = Setup(B, wl)
+    y_g, _ = _forward(B, st, tile_n=tile_n)
+    ref = O.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, wl.k)
+    Hp.assert_bf16_close(y_g, ref["y"], what=f"tiny tile_n={tile_n}")
