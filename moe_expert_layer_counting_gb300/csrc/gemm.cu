@@ -62,14 +62,20 @@ constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in H
 // N <= 64, with one K block per stage where shared memory is tight), giving
 // the SM independent MMA issue streams without changing any accumulation
 // order.
-template <int BN>
+// (c) GEMM2 with 224-token tiles runs two CTAs per SM with one TMEM
+// accumulator each (2 x 224 columns would not fit twice): its light BF16
+// epilogue is not overlapped with the CTA's own MMAs but with the other
+// CTA's, and the second issue stream pays for that; GEMM1's SwiGLU and
+// requantisation epilogue is too long for it.
+template <int BN, int PHASE = 1>
 struct Cfg {
+  static constexpr bool kWideTwoCta = BN > 128 && PHASE == 2;
   // tiles above 128 tokens: scales of the token operand in two 128-row
   // groups, and an 8-warp epilogue (two warps per TMEM quadrant)
-  static constexpr int kKBS = (BN == 16 || BN == 64) ? 1 : 2;
-  static constexpr int kCtasPerSm = BN == 16 ? 3 : (BN <= 64 ? 2 : 1);
+  static constexpr int kKBS = (BN == 16 || BN == 64 || kWideTwoCta) ? 1 : 2;
+  static constexpr int kCtasPerSm = BN == 16 ? 3 : (BN <= 64 || kWideTwoCta ? 2 : 1);
   // accumulators in TMEM (two: the epilogue of one item overlaps the MMAs of the next)
-  static constexpr int kAccBufs = 2;
+  static constexpr int kAccBufs = kWideTwoCta ? 1 : 2;
   static constexpr int kSfbGroups = (BN + 127) / 128;       // 128-row groups of token scales
   static constexpr int kTokChunk = 512 * kSfbGroups;        // bytes of one (tile, K block) token-scale chunk
   static constexpr int kSfSlot = 4 + 4 * kSfbGroups;        // TMEM columns of one K block's scales
@@ -105,9 +111,9 @@ struct Cfg {
   static_assert(kTmemAlloc * kCtasPerSm <= 512, "co-resident CTAs share the SM's 512 TMEM columns");
 };
 
-template <int BN>
+template <int BN, int PHASE = 1>
 size_t smem_bytes(int E) {
-  return 1024 + Cfg<BN>::kOffExp + (size_t)3 * (E + 1) * 4;
+  return 1024 + Cfg<BN, PHASE>::kOffExp + (size_t)3 * (E + 1) * 4;
 }
 
 struct GemmArgs {
@@ -198,14 +204,14 @@ __device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int 
 #endif
 
 template <int BN, int PHASE>
-__global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
+__global__ void __launch_bounds__(Cfg<BN, PHASE>::kThreads, Cfg<BN, PHASE>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_b2,
                        const GemmArgs args) {
   // PHASE 1: GEMM1 + SwiGLU epilogue; 2: GEMM2; 3: both and the combine in
   // one launch (small problems): GEMM1 items, then GEMM2 items (each waiting
   // on the GEMM1 items of its token tile), then the combine
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PHASE>;
   constexpr bool kFused = PHASE == 3;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1020,10 +1026,11 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   }
   if (phases & MOE_PHASE_GEMM2) {
     // GEMM2 -> BF16 per pair
+    using C2 = Cfg<BN, 2>;
     const uint64_t wrows = (uint64_t)E * (a->H / 128) * (a->I / 128) * 128;
     CUtensorMap tw2, th;
     bool ok = encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, 128, wrows, 64, 128,
-                             C::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+                             C2::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
                               (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
@@ -1031,8 +1038,10 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     g.w_sf = a->w2s; g.b_sf = sfb2;
     g.early_weights = (phases & MOE_PHASE_GEMM1) ? 1 : 0;
     g.hs_out = nullptr;
-    if (!set_gemm_attrs(expert_gemm_kernel<BN, 2>, sm)) return MOE_ERR_CUDA;
-    if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(grid), dim3(C::kThreads), sm, st, tw2, th, tw2, th, g) != MOE_OK)
+    const size_t sm2 = smem_bytes<BN, 2>(E);
+    if (!set_gemm_attrs(expert_gemm_kernel<BN, 2>, sm2)) return MOE_ERR_CUDA;
+    if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(num_sms() * C2::kCtasPerSm), dim3(C2::kThreads), sm2, st, tw2, th,
+                   tw2, th, g) != MOE_OK)
       return MOE_ERR_CUDA;
   }
   return MOE_OK;
