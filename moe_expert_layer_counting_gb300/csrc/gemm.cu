@@ -62,14 +62,13 @@ constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in H
 // N <= 64, with one K block per stage where shared memory is tight), giving
 // the SM independent MMA issue streams without changing any accumulation
 // order.
-// (c) GEMM2 with 224-token tiles runs two CTAs per SM with one TMEM
-// accumulator each (2 x 224 columns would not fit twice): its light BF16
-// epilogue is not overlapped with the CTA's own MMAs but with the other
-// CTA's, and the second issue stream pays for that; GEMM1's SwiGLU and
-// requantisation epilogue is too long for it.
-template <int BN, int PHASE = 1>
+// (c) 224-token tiles run two CTAs per SM with one TMEM accumulator each
+// (2 x 224 columns would not fit twice): a CTA's epilogue is not overlapped
+// with its own MMAs but with the other CTA's, and the second issue stream
+// pays for that (GEMM1 -9 %, GEMM2 -13 % on the prefill, measured).
+template <int BN>
 struct Cfg {
-  static constexpr bool kWideTwoCta = BN > 128 && PHASE == 2;
+  static constexpr bool kWideTwoCta = BN > 128;
   // tiles above 128 tokens: scales of the token operand in two 128-row
   // groups, and an 8-warp epilogue (two warps per TMEM quadrant)
   static constexpr int kKBS = (BN == 16 || BN == 64 || kWideTwoCta) ? 1 : 2;
@@ -111,9 +110,9 @@ struct Cfg {
   static_assert(kTmemAlloc * kCtasPerSm <= 512, "co-resident CTAs share the SM's 512 TMEM columns");
 };
 
-template <int BN, int PHASE = 1>
+template <int BN>
 size_t smem_bytes(int E) {
-  return 1024 + Cfg<BN, PHASE>::kOffExp + (size_t)3 * (E + 1) * 4;
+  return 1024 + Cfg<BN>::kOffExp + (size_t)3 * (E + 1) * 4;
 }
 
 struct GemmArgs {
@@ -204,14 +203,14 @@ __device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int 
 #endif
 
 template <int BN, int PHASE>
-__global__ void __launch_bounds__(Cfg<BN, PHASE>::kThreads, Cfg<BN, PHASE>::kCtasPerSm)
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_b2,
                        const GemmArgs args) {
   // PHASE 1: GEMM1 + SwiGLU epilogue; 2: GEMM2; 3: both and the combine in
   // one launch (small problems): GEMM1 items, then GEMM2 items (each waiting
   // on the GEMM1 items of its token tile), then the combine
-  using C = Cfg<BN, PHASE>;
+  using C = Cfg<BN>;
   constexpr bool kFused = PHASE == 3;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -554,20 +553,29 @@ __global__ void __launch_bounds__(Cfg<BN, PHASE>::kThreads, Cfg<BN, PHASE>::kCta
             }
           }
           named_bar_sync(bar_half, 128);
-          // requantise: 16 columns x 2 groups of 32 features, 8 items per warp
-#pragma unroll 1
-          for (int it = q; it < 2 * kChunk; it += 4) {
+          // requantise: 16 columns x 2 groups of 32 features = 32 items; an
+          // 8-lane group takes one item, 4 features per lane (one 16-byte
+          // read, a 3-step xor max, one 4-byte store), 4 items per warp pass
+#pragma unroll
+          for (int pass = 0; pass < 2; ++pass) {
+            const int it = q * 8 + pass * 4 + (lane >> 3);
             const int col = it >> 1, grp = it & 1;
             const int c = c0 + col;
-            if (c >= ti.valid) continue;                              // warp-uniform
-            const float h = ebuf_f[col * 64 + grp * 32 + lane];
-            const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
-            const int e = ue8m0_exponent<true>(__uint_as_float(amax_bits));
-            const uint8_t code = (uint8_t)(cvt_e4m3x2(h * pow2_neg(e), 0.f) & 0xFFu);
+            const int f4 = (lane & 7) * 4;                            // this lane's first feature in the group
+            const float4 hv = *reinterpret_cast<const float4 *>(ebuf_f + col * 64 + grp * 32 + f4);
+            float amax = fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w)));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+            if (c >= ti.valid) continue;                              // uniform in the 8-lane group
+            const int e = ue8m0_exponent<true>(amax);
+            const float inv = pow2_neg(e);
+            const uint32_t codes = (uint32_t)cvt_e4m3x2(hv.x * inv, hv.y * inv) |
+                                   ((uint32_t)cvt_e4m3x2(hv.z * inv, hv.w * inv) << 16);
             const size_t s = (size_t)(ti.s0 + c);
             const int fcol = ti.mt * 64 + grp * 32;                  // first feature of the group
-            args.hq[s * args.I + fcol + lane] = code;
-            if (lane == 0) {
+            *reinterpret_cast<uint32_t *>(args.hq + s * args.I + fcol + f4) = codes;
+            if ((lane & 7) == 0) {
               const int fg = fcol >> 5;                               // 32-group index along I
               const size_t chunk = (size_t)ti.g * (args.I / 128) + (fg >> 2);
               const int cr = c & 127;
@@ -1026,11 +1034,10 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
   }
   if (phases & MOE_PHASE_GEMM2) {
     // GEMM2 -> BF16 per pair
-    using C2 = Cfg<BN, 2>;
     const uint64_t wrows = (uint64_t)E * (a->H / 128) * (a->I / 128) * 128;
     CUtensorMap tw2, th;
     bool ok = encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, 128, wrows, 64, 128,
-                             C2::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+                             C::kKBS * kBM, CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
                               (uint64_t)a->I, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return MOE_ERR_CUDA;
@@ -1038,10 +1045,8 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
     g.w_sf = a->w2s; g.b_sf = sfb2;
     g.early_weights = (phases & MOE_PHASE_GEMM1) ? 1 : 0;
     g.hs_out = nullptr;
-    const size_t sm2 = smem_bytes<BN, 2>(E);
-    if (!set_gemm_attrs(expert_gemm_kernel<BN, 2>, sm2)) return MOE_ERR_CUDA;
-    if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(num_sms() * C2::kCtasPerSm), dim3(C2::kThreads), sm2, st, tw2, th,
-                   tw2, th, g) != MOE_OK)
+    if (!set_gemm_attrs(expert_gemm_kernel<BN, 2>, sm)) return MOE_ERR_CUDA;
+    if (launch_pdl(expert_gemm_kernel<BN, 2>, dim3(grid), dim3(C::kThreads), sm, st, tw2, th, tw2, th, g) != MOE_OK)
       return MOE_ERR_CUDA;
   }
   return MOE_OK;
