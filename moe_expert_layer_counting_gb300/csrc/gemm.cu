@@ -139,7 +139,7 @@ struct GemmArgs {
   // GEMM1 + GEMM2 + combine in one launch (PHASE 3): GEMM2's operands, the
   // arrival counters and the combine
   int MT2, KB2;
-  const uint8_t *w_sf2, *b_sf2;
+  const uint8_t *w_sf2, *b_sf2, *w_codes2;
   int *sync;                        // [0] GEMM2 items done, [1 + g] GEMM1 items of token tile g done
   const int32_t *topk_idx;          // [T][k] (combine: dropped slots skipped)
   uint4 *y;                         // [T][H] bf16 (combine output)
@@ -387,6 +387,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
           if (lane == 0) {
             issue_weights(stage, kb, min(C::kKBS, it.KB - kb), wtile, it);
             issue_tokens(stage, kb, min(C::kKBS, it.KB - kb), it);
+            if (kb + kPrefetchAhead < it.KB)
+              prefetch_l2_bulk((it.l1 ? args.w_codes : args.w_codes2) + ((size_t)wtile + kb + kPrefetchAhead) * kWTileBytes,
+                               kWTileBytes);
           }
           __syncwarp();
           advance();
@@ -1146,6 +1149,7 @@ int launch_fused_gemms(const moe_expert_args *a, uint16_t *y, int *sync, int *st
   g.tok_pool = reinterpret_cast<int32_t *>(ews + lay.tok_pool);
   g.w_pool = reinterpret_cast<float *>(ews + lay.w_pool);
   g.w_sf = a->w1s; g.b_sf = sfb1; g.w_sf2 = a->w2s; g.b_sf2 = sfb2; g.w_codes = a->w1q;
+  g.w_codes2 = a->w2q;
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = nullptr; g.y_pairs = a->y_pairs; g.status = status;
   g.sync = sync; g.topk_idx = a->topk_idx; g.y = reinterpret_cast<uint4 *>(y);
   if (const char *env = getenv("MOE_MXQ_DEBUG_INJECT_WAIT")) g.inject_wait = atoi(env);
