@@ -63,13 +63,14 @@ constexpr int kPrefetchAhead = 2;             // K blocks between an L2 prefetch
 // N <= 64, with one K block per stage where shared memory is tight), giving
 // the SM independent MMA issue streams without changing any accumulation
 // order.
-// (c) 224-token tiles run two CTAs per SM with one TMEM accumulator each
-// (2 x 224 columns would not fit twice): a CTA's epilogue is not overlapped
-// with its own MMAs but with the other CTA's, and the second issue stream
-// pays for that (GEMM1 -9 %, GEMM2 -13 % on the prefill, measured).
+// (c) 128- and 224-token tiles run two CTAs per SM with one TMEM accumulator
+// each (two accumulators would not fit twice): a CTA's epilogue is not
+// overlapped with its own MMAs but with the other CTA's, and the second
+// issue stream pays for that (224: GEMM1 -9 %, GEMM2 -13 % on the prefill;
+// 128: -7 % / -16 %, measured).
 template <int BN>
 struct Cfg {
-  static constexpr bool kWideTwoCta = BN > 128;
+  static constexpr bool kWideTwoCta = BN >= 128;
   // tiles above 128 tokens: scales of the token operand in two 128-row
   // groups, and an 8-warp epilogue (two warps per TMEM quadrant)
   static constexpr int kKBS = (BN == 16 || BN == 64 || kWideTwoCta) ? 1 : 2;
@@ -88,7 +89,8 @@ struct Cfg {
   static constexpr int kBBytes = kKBS * kBTile;
   static constexpr int kSfbBytes = BN < 32 ? BN * 16 : kTokChunk;   // used bytes of a token-scale chunk
   static constexpr int kStageBytes = kABytes + kBBytes + kKBS * (512 + kTokChunk);
-  static constexpr int kSmemBudget = (kCtasPerSm == 1 ? 200 : kCtasPerSm == 2 ? 96 : 60) * 1024;
+  // (128-token tiles: three 33 KB stages in two CTAs' share of the SM)
+  static constexpr int kSmemBudget = (kCtasPerSm == 1 ? 200 : kCtasPerSm == 2 ? (BN == 128 ? 100 : 96) : 60) * 1024;
   static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
   static constexpr int kTmemCols = kAccBufs * BN + kSfSlot * kKBS * kStages;
   static constexpr uint32_t kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
