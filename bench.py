@@ -44,11 +44,11 @@ METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM G
 # those sources change.
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC = {
-    "src_sha256": "569750d60b7ebe9b861ead1797afac4f2febc3b1695a8c4ff1325e9a818b1711",
-    "small_decode": {"gemm1": 62791680 + 12032, "gemm2": 31326464 + 0},
-    "large_decode": {"gemm1": 3959697408 + 2406912, "gemm2": 1976327680 + 13979904},
-    "prefill": {"gemm1": 4244078592 + 67489280, "gemm2": 2068602112 + 451102208},
-    "skewed_prefill": {"gemm1": 3183461888 + 139540992, "gemm2": 1335301888 + 939533824},
+    "src_sha256": "bd6690ba1d8da7b85101f9a770f57f3ca587cd717d4b65fa525b39013212f676",
+    "small_decode": {"gemm1": 62794496 + 2048, "gemm2": 31327744 + 0},
+    "large_decode": {"gemm1": 3959589888 + 2434816, "gemm2": 1976362752 + 14259968},
+    "prefill": {"gemm1": 4272065792 + 67646464, "gemm2": 2068049920 + 449129472},
+    "skewed_prefill": {"gemm1": 3272554240 + 140031744, "gemm2": 1335592960 + 939598336},
 }
 UNIT = "tokens/s"
 
