@@ -44,7 +44,7 @@ METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM G
 # those sources change.
 GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC = {
-    "src_sha256": "bd6690ba1d8da7b85101f9a770f57f3ca587cd717d4b65fa525b39013212f676",
+    "src_sha256": "34049e5ab0ee6b69086c8a0d5539f70af5e8ef42ab113637067f39a5008b6996",
     "small_decode": {"gemm1": 62794496 + 2048, "gemm2": 31327744 + 0},
     "large_decode": {"gemm1": 3959589888 + 2434816, "gemm2": 1976362752 + 14259968},
     "prefill": {"gemm1": 4272065792 + 67646464, "gemm2": 2068049920 + 449129472},

@@ -6,24 +6,27 @@
 // then GEMM2 (FP8 h x FP4 W2) with a BF16 epilogue that scatters each pair's
 // row to y_pairs[slot][token].
 //
-// Prior art: MegaMoE (study notes), "Warp roles", "Scheduler", "L1
+// Prior art: MegaMoE (study notes), "Warp roles", "Scheduler", "Wave", "L1
 // epilogue", "L2 epilogue" and the gate/up interleave; Warp Specialization:
 // DeepEP vs Mega MoE (MMA issue with the weights in the M slot, UTCCP copy of
 // the scale factors into TMEM, epilogue listings).  What is kept on sm_103a:
 //   * weights are the MMA's M operand (128 rows per tile) and tokens the N
-//     operand (16..128 per tile), so decode-sized experts waste little MMA;
-//   * one persistent CTA per SM, warp roles: warp 0 TMA producer, warp 1
-//     TMEM allocator + single-thread MMA issuer, warps 2-5 epilogue (one TMEM
-//     lane quadrant each);
-//   * a ring of shared-memory stages (full/empty mbarriers) and two TMEM
-//     accumulators (tmem_full/tmem_empty) so loads, MMAs and the epilogue of
-//     consecutive tiles overlap;
+//     operand (16..224 per tile), so decode-sized experts waste little MMA;
+//   * persistent CTAs (one to three per SM, see Cfg), warp roles: warp 0 TMA
+//     producer, warp 1 TMEM allocator + single-thread MMA issuer, warps 2-5
+//     (2-9) epilogue (one TMEM lane quadrant each);
+//   * a ring of shared-memory stages (full/empty mbarriers) and one or two
+//     TMEM accumulators (tmem_full/tmem_empty) so loads, MMAs and epilogues
+//     overlap;
 //   * FP4 weights are unpacked into 8-bit containers by TMA
-//     (16U4_ALIGN16B, 128B swizzle); token rows of GEMM1 are gathered from
-//     the un-permuted FP8 activations with TMA tile::gather4 by pair id,
-//     which replaces the pages' NVLink pull into a pool buffer;
+//     (16U4_ALIGN16B, 128B swizzle); token rows come from an expert-major
+//     pool of FP8 rows in HBM, which replaces the pages' NVLink pull into a
+//     pool buffer;
 //   * scale factors travel as 512-byte chunks already in the tcgen05.cp
-//     32x128b.warpx4 order and land in TMEM next to the accumulators.
+//     32x128b.warpx4 order and land in TMEM next to the accumulators;
+//   * small problems run GEMM1, GEMM2 and the combine in one launch, GEMM2
+//     items waiting on per-token-tile arrival counters (the pages' arrival
+//     mask), all bounded.
 // Not kept: the dispatch warps and NVLink stores (one GPU), the 2-SM
 // cluster, and unbounded spins (every wait here gives up after ~1 s and
 // reports MOE_ERR_TIMEOUT through the workspace status word).
