@@ -10,4 +10,4 @@ Every function is pinned in ``tests/test_oracle_*.py`` to something other than
 itself: hand-computed encodings (``tests/golden/``), brute force on small
 inputs, closed forms and invariants.
 """
-from . import formats, moe  # noqa: F401
+from . import bfp8, formats, moe  # noqa: F401
