@@ -1,6 +1,7 @@
 """ctypes binding of libmoe_mxq.so -- argument marshalling only.
 
-Every function has the name of the C entry point it calls (include/moe_mxq.h)
+Every function has the name of the C entry point it calls (include/moe_mxq.h,
+include/moe_bfp8.h)
 and takes torch tensors for the device buffers; all work runs in the
 library's CUDA kernels on the given (default: current) stream.  PyTorch is
 used for device memory and streams only.  A non-zero status raises MoeError.
@@ -44,7 +45,8 @@ ROUTE_SOFTMAX, ROUTE_SIGMOID, ROUTE_RAW, ROUTE_NO_RENORM = 0, 1, 2, 4
 EXPORTED = ["mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_route_topk_ex",
             "moe_permute_workspace_size",
             "moe_permute", "moe_permute_noalloc", "moe_expert_workspace_size", "moe_expert_forward", "moe_combine",
-            "moe_workspace_size", "moe_forward", "moe_get_device_status", "moe_status_string", "moe_version"]
+            "moe_workspace_size", "moe_forward", "moe_get_device_status", "moe_status_string", "moe_version",
+            "bfp8_quantize_act", "bfp8_quantize_weight", "moe_bfp8_workspace_size", "moe_forward_bfp8"]
 
 
 class MoeExpertArgs(ctypes.Structure):
@@ -74,6 +76,16 @@ class MoeForwardArgs(ctypes.Structure):
                 ("route_mode", _i32)]
 
 
+class MoeBfp8Args(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_uint32),
+                ("T", _i64), ("H", _i64), ("I", _i64),
+                ("E", _i32), ("k", _i32), ("route_mode", _i32),
+                ("x", _p), ("logits", _p), ("w1q", _p), ("w1s", _p), ("w2q", _p), ("w2s", _p), ("y", _p),
+                ("topk_idx_out", _p), ("topk_w_out", _p), ("counts_out", _p), ("offsets_out", _p),
+                ("perm_out", _p), ("hq_out", _p), ("hs_out", _p),
+                ("workspace", _p), ("workspace_bytes", _sz)]
+
+
 lib.mxq_quantize_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
 lib.mxq_quantize_weight.argtypes = [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _p]
 lib.moe_route_topk.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p]
@@ -89,6 +101,11 @@ lib.moe_combine.argtypes = [_p, _p, _i64, _i32, _i64, _p, _p]
 lib.moe_workspace_size.argtypes = [_i64, _i64, _i64, _i32, _i32]
 lib.moe_workspace_size.restype = _sz
 lib.moe_forward.argtypes = [ctypes.POINTER(MoeForwardArgs), _p]
+lib.bfp8_quantize_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
+lib.bfp8_quantize_weight.argtypes = [_p, _i64, _i64, _i64, _p, _p, _p]
+lib.moe_bfp8_workspace_size.argtypes = [_i64, _i64, _i64, _i32, _i32]
+lib.moe_bfp8_workspace_size.restype = _sz
+lib.moe_forward_bfp8.argtypes = [ctypes.POINTER(MoeBfp8Args), _p]
 lib.moe_get_device_status.argtypes = [_p, _p, ctypes.POINTER(ctypes.c_int)]
 lib.moe_status_string.argtypes = [ctypes.c_int]
 lib.moe_status_string.restype = ctypes.c_char_p
@@ -96,7 +113,8 @@ lib.moe_version.restype = ctypes.c_char_p
 for _name in ("mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_route_topk_ex", "moe_permute",
               "moe_permute_noalloc",
               "moe_expert_forward",
-              "moe_combine", "moe_forward", "moe_get_device_status"):
+              "moe_combine", "moe_forward", "moe_get_device_status", "bfp8_quantize_act", "bfp8_quantize_weight",
+              "moe_forward_bfp8"):
     getattr(lib, _name).restype = ctypes.c_int
 
 
@@ -242,3 +260,43 @@ def moe_get_device_status(workspace: torch.Tensor, stream=None) -> int:
     _check(lib.moe_get_device_status(_ptr(workspace), _stream(stream), ctypes.byref(out)),
            "moe_get_device_status")
     return int(out.value)
+
+
+# ---------------------------------------------------------------- block-FP8 variant (include/moe_bfp8.h)
+
+def bfp8_quantize_act(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None, check=True) -> int:
+    """x bf16 [rows, K] -> q uint8 [rows, K] (E4M3), s float32 [rows, K/128]."""
+    rows, K = x.shape
+    rc = lib.bfp8_quantize_act(_ptr(x), rows, K, _ptr(q), _ptr(s), _stream(stream))
+    if check:
+        _check(rc, "bfp8_quantize_act")
+    return rc
+
+
+def bfp8_quantize_weight(w: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None, check=True) -> int:
+    """w bf16 [G, N, K] -> q uint8 [G, N, K] (E4M3), s float32 [G, N/128, K/128]."""
+    G, N, K = w.shape
+    rc = lib.bfp8_quantize_weight(_ptr(w), G, N, K, _ptr(q), _ptr(s), _stream(stream))
+    if check:
+        _check(rc, "bfp8_quantize_weight")
+    return rc
+
+
+def moe_bfp8_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
+    return int(lib.moe_bfp8_workspace_size(T, H, I, E, k))
+
+
+def moe_forward_bfp8(x, logits, w1q, w1s, w2q, w2s, k: int, y, workspace, topk_idx_out=None, topk_w_out=None,
+                     counts_out=None, offsets_out=None, perm_out=None, hq_out=None, hs_out=None,
+                     route_mode: int = ROUTE_SOFTMAX, stream=None, check=True) -> int:
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w2q.shape[2]
+    a = MoeBfp8Args(ctypes.sizeof(MoeBfp8Args), T, H, I, E, k, route_mode,
+                    _ptr(x), _ptr(logits), _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s), _ptr(y),
+                    _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), _ptr(offsets_out), _ptr(perm_out),
+                    _ptr(hq_out), _ptr(hs_out), _ptr(workspace), workspace.numel() * workspace.element_size())
+    rc = lib.moe_forward_bfp8(ctypes.byref(a), _stream(stream))
+    if check:
+        _check(rc, "moe_forward_bfp8")
+    return rc

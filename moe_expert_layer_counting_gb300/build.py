@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_mxq.so")
-SOURCES = ["quant.cu", "route.cu", "permute.cu", "permute_noalloc.cu", "gemm.cu", "combine.cu", "api.cu"]
+SOURCES = ["quant.cu", "route.cu", "permute.cu", "permute_noalloc.cu", "gemm.cu", "combine.cu", "api.cu", "bfp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -41,6 +41,7 @@ def _newest(paths):
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     files.append(os.path.join(INCLUDE, "moe_mxq.h"))
+    files.append(os.path.join(INCLUDE, "moe_bfp8.h"))
     files.append(os.path.abspath(__file__))
     return files
 

@@ -13,17 +13,19 @@ import pytest
 from tests import helpers as Hp
 
 HEADER = os.path.join(Hp.ROOT, "include", "moe_mxq.h")
+HEADERS = [os.path.join(Hp.ROOT, "include", h) for h in sorted(os.listdir(os.path.join(Hp.ROOT, "include")))
+           if h.endswith(".h")]
 
 
 def _declared():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"MOE_API\s+(?:const\s+char\s*\*|int|size_t)\s*(\w+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_symbol():
     B = Hp.lib()
     names = _declared()
-    assert len(names) >= 13
+    assert len(names) >= 19 and "moe_forward_bfp8" in names
     for n in names:
         assert hasattr(B.lib, n), n
     assert set(names) == set(B.EXPORTED)
@@ -97,3 +99,60 @@ def test_workspace_sizes_grow_with_the_problem():
     assert big >= 4096 * 8 * 7168 * 2
     assert B.moe_expert_workspace_size(64, 256, 128, 8, 2) > 0
     assert B.moe_permute_workspace_size(8192, 256, 8) >= 256 + 32 * 256 * 4
+
+
+def test_bfp8_struct_layout_matches_c(tmp_path):
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    src = tmp_path / "sz.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "moe_bfp8.h"\n'
+        'int main(void){printf("%zu %zu %zu %zu %zu\\n", sizeof(moe_bfp8_args), offsetof(moe_bfp8_args, route_mode),'
+        ' offsetof(moe_bfp8_args, x), offsetof(moe_bfp8_args, hs_out), offsetof(moe_bfp8_args, workspace_bytes));'
+        ' return 0;}\n')
+    exe = tmp_path / "sz"
+    subprocess.run([cc, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    B = Hp.lib()
+    A = B.MoeBfp8Args
+    assert got == [ctypes.sizeof(A), A.route_mode.offset, A.x.offset, A.hs_out.offset, A.workspace_bytes.offset]
+
+
+def test_bfp8_host_validation_rejects_bad_arguments():
+    B = Hp.lib()
+    L = B.lib
+    s0 = ctypes.c_void_p(0)
+    p = ctypes.c_void_p(0x1000)
+    assert L.bfp8_quantize_act(p, -1, 128, p, p, s0) == B.MOE_ERR_INVALID_ARG
+    assert L.bfp8_quantize_act(p, 4, 96, p, p, s0) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.bfp8_quantize_act(None, 4, 128, p, p, s0) == B.MOE_ERR_INVALID_ARG
+    assert L.bfp8_quantize_act(p, 4, 128, p, ctypes.c_void_p(0x1002), s0) == B.MOE_ERR_MISALIGNED
+    assert L.bfp8_quantize_act(p, 4, 128, ctypes.c_void_p(0x1004), p, s0) == B.MOE_ERR_MISALIGNED
+    assert L.bfp8_quantize_act(p, 0, 128, p, p, s0) == B.MOE_OK
+    assert L.bfp8_quantize_weight(p, 1, 64, 128, p, p, s0) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.bfp8_quantize_weight(p, -1, 128, 128, p, p, s0) == B.MOE_ERR_INVALID_ARG
+    assert L.bfp8_quantize_weight(p, 0, 128, 128, p, p, s0) == B.MOE_OK
+    assert L.moe_bfp8_workspace_size(-1, 128, 128, 4, 2) == 0
+    assert L.moe_bfp8_workspace_size(8, 2048, 512, 256, 8) > 8 * 8 * 2048 * 4
+    a = B.MoeBfp8Args()
+    a.struct_size = 7
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG
+    a.struct_size = ctypes.sizeof(a)
+    a.T, a.H, a.I, a.E, a.k = 8, 192, 128, 4, 2
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_UNSUPPORTED_SHAPE      # H % 128
+    a.H, a.k = 256, 5
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_UNSUPPORTED_SHAPE      # k > E
+    a.k, a.route_mode = 2, 3
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG            # bad routing mode
+    a.route_mode = 0
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG            # no workspace
+    a.workspace = ctypes.c_void_p(0x1080)
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_MISALIGNED
+    a.workspace, a.workspace_bytes = ctypes.c_void_p(0x10000), 64
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    a.workspace_bytes = L.moe_bfp8_workspace_size(8, 256, 128, 4, 2)
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG            # null tensors
+    a.x = a.logits = a.y = a.w1q = a.w1s = a.w2q = a.w2s = p
+    a.y = ctypes.c_void_p(0x1008)
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_MISALIGNED
