@@ -2,6 +2,7 @@
 """Benchmark of the MoE expert layer (moe_forward) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--weights fp4|bfp8]
 
 One step = one moe_forward (activation cast, routing, counting-sort permute,
 GEMM1 + SwiGLU (.) weight + FP8 requantisation, GEMM2, combine) over the
@@ -19,6 +20,10 @@ max-over-ranks time, "scaling": "weak".
 
 --impl reference times the CPU oracle (oracle/, float64) on this host's cores
 on a fixed 2-token sample of the same workload (rank 0 only).
+
+--weights bfp8 times the block-FP8 variant instead (moe_forward_bfp8: E4M3
+weights with 128 x 128 block scales, per-128 token scales), on the same
+workload shapes and inputs.
 """
 from __future__ import annotations
 
@@ -50,6 +55,11 @@ TRAFFIC = {
     "prefill": {"gemm1": 4272065792 + 67646464, "gemm2": 2068049920 + 449129472},
     "skewed_prefill": {"gemm1": 3272554240 + 140031744, "gemm2": 1335592960 + 939598336},
 }
+# the same for the block-FP8 variant's GEMMs (csrc/bfp8.cu)
+BFP8_SOURCES = ("bfp8.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
+TRAFFIC_BFP8 = {
+    "src_sha256": None,
+}
 UNIT = "tokens/s"
 
 
@@ -61,6 +71,8 @@ def parse():
     ap.add_argument("--workload", default="small_decode")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--weights", default="fp4", choices=["fp4", "bfp8"],
+                    help="fp4: FP8 x FP4 with UE8M0 per 32 (moe_forward); bfp8: block-FP8 weights (moe_forward_bfp8)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (for profiler launch lists)")
     ap.add_argument("--quick", action="store_true", help="skip the CPU-baseline and e2e legs")
     ap.add_argument("--launch-list", action="store_true",
@@ -138,20 +150,21 @@ def gpu_id_for(dev) -> str:
 
 # ---------------------------------------------------------------- roofline bookkeeping
 
-def gemm_sources_sha256():
+def gemm_sources_sha256(sources=GEMM_SOURCES):
     import hashlib
     h = hashlib.sha256()
     base = os.path.join(os.path.dirname(os.path.abspath(__file__)), "moe_expert_layer_counting_gb300", "csrc")
-    for name in GEMM_SOURCES:
+    for name in sources:
         with open(os.path.join(base, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def measured_traffic(workload, phase):
-    """Bytes per launch from the ncu table above, or None if stale or not captured."""
-    entry = TRAFFIC.get(workload, {})
-    if TRAFFIC.get("src_sha256") != gemm_sources_sha256() or phase not in entry:
+def measured_traffic(workload, phase, bfp8=False):
+    """Bytes per launch from the ncu tables above, or None if stale or not captured."""
+    table, sources = (TRAFFIC_BFP8, BFP8_SOURCES) if bfp8 else (TRAFFIC, GEMM_SOURCES)
+    entry = table.get(workload, {})
+    if table.get("src_sha256") != gemm_sources_sha256(sources) or phase not in entry:
         return None
     return entry[phase]
 
@@ -186,6 +199,28 @@ def algorithmic(wl, counts):
     }
 
 
+def algorithmic_bfp8(wl, counts):
+    """The same for the block-FP8 variant: one byte per weight plus one float32
+    scale per 128 x 128 block; FP8 tokens and h with one float32 scale per 128;
+    GEMM2 writes FP32 pair rows."""
+    touched = int((counts > 0).sum())
+    P = wl.T * wl.k
+    w1 = 2 * wl.I * wl.H + (2 * wl.I // 128) * (wl.H // 128) * 4
+    w2 = wl.H * wl.I + (wl.H // 128) * (wl.I // 128) * 4
+    x_q = wl.T * (wl.H + wl.H // 128 * 4)
+    h_q = P * (wl.I + wl.I // 128 * 4)
+    y_pairs = P * wl.H * 4
+    return {
+        "touched_experts": touched,
+        "layer_bytes": wl.T * wl.H * 2 + wl.T * wl.E * 4 + touched * (w1 + w2) + wl.T * wl.H * 2,
+        "layer_flops": 2 * P * 3 * wl.H * wl.I,
+        "gemm1_bytes": touched * w1 + x_q + h_q,
+        "gemm1_flops": 2 * P * 2 * wl.I * wl.H,
+        "gemm2_bytes": touched * w2 + h_q + y_pairs,
+        "gemm2_flops": 2 * P * wl.H * wl.I,
+    }
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -203,13 +238,25 @@ def run_ours(args, rank, world, local_rank):
     x_cpu, logits_cpu = W.tokens(wl)
     x = x_cpu.to(dev)
     logits = logits_cpu.to(dev)
-    qe = QuantizedExperts(wl.E, wl.H, wl.I, device=dev)
-    for e in range(wl.E):
-        l1, l2 = W.expert_weights(wl, e, dev)
-        qe.set_expert(e, l1, l2)
-    del l1, l2
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
-    ws = torch.empty(B.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    bfp8 = args.weights == "bfp8"
+    if bfp8:
+        w1q = torch.empty(E, 2 * I, H, dtype=torch.uint8, device=dev)
+        w1s = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32, device=dev)
+        w2q = torch.empty(E, H, I, dtype=torch.uint8, device=dev)
+        w2s = torch.empty(E, H // 128, I // 128, dtype=torch.float32, device=dev)
+        for e in range(E):
+            l1, l2 = W.expert_weights(wl, e, dev)
+            B.bfp8_quantize_weight(l1[None], w1q[e:e + 1], w1s[e:e + 1])
+            B.bfp8_quantize_weight(l2[None], w2q[e:e + 1], w2s[e:e + 1])
+        ws = torch.empty(B.moe_bfp8_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    else:
+        qe = QuantizedExperts(wl.E, wl.H, wl.I, device=dev)
+        for e in range(wl.E):
+            l1, l2 = W.expert_weights(wl, e, dev)
+            qe.set_expert(e, l1, l2)
+        ws = torch.empty(B.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    del l1, l2
     y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     idx = torch.empty(T, k, dtype=torch.int32, device=dev)
     wts = torch.empty(T, k, dtype=torch.float32, device=dev)
@@ -221,8 +268,12 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
 
     def forward(st):
-        B.moe_forward(x, logits, qe.w1q, qe.w1s, qe.w2q, qe.w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
-                      counts_out=counts, offsets_out=offsets, perm_out=perm, tile_n=args.tile_n, stream=st)
+        if bfp8:
+            B.moe_forward_bfp8(x, logits, w1q, w1s, w2q, w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
+                               counts_out=counts, offsets_out=offsets, perm_out=perm, stream=st)
+        else:
+            B.moe_forward(x, logits, qe.w1q, qe.w1s, qe.w2q, qe.w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
+                          counts_out=counts, offsets_out=offsets, perm_out=perm, tile_n=args.tile_n, stream=st)
 
     def flush():
         if not args.no_flush:
@@ -237,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.graph(graph, stream=stream):
         forward(torch.cuda.current_stream())
     counts_np = counts.cpu().numpy()
-    n_launch_forward = launches_per_forward(T, H, E, k)
+    n_launch_forward = launches_per_forward_bfp8(T, H, E, k) if bfp8 else launches_per_forward(T, H, E, k)
 
     def timed_loop(step_fn, steps):
         evs = []
@@ -284,19 +335,26 @@ def run_ours(args, rank, world, local_rank):
         value = world * T * args.steps / (total_ms / 1e3)
 
     # per-GEMM timing (dominant kernel) with the layer's own routing
-    ews = torch.empty(B.moe_expert_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
-    xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
-    xs = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
-    y_pairs = torch.empty(k, T, H, dtype=torch.bfloat16, device=dev)
-    with torch.cuda.stream(stream):
-        B.mxq_quantize_act(x, xq, xs, stream=stream)
+    if bfp8:
+        ews = ws                              # the GEMMs re-run on the state the forward left
 
-    def phase(ph):
-        B.moe_expert_forward(xq, xs, qe.w1q, qe.w1s, qe.w2q, qe.w2s, idx, wts, counts, offsets, perm, y_pairs,
-                             ews, tile_n=args.tile_n, phases=ph, stream=stream)
+        def phase(ph):
+            B.moe_forward_bfp8(x, logits, w1q, w1s, w2q, w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
+                               counts_out=counts, offsets_out=offsets, perm_out=perm, phases=ph, stream=stream)
+    else:
+        ews = torch.empty(B.moe_expert_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+        xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
+        xs = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+        y_pairs = torch.empty(k, T, H, dtype=torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            B.mxq_quantize_act(x, xq, xs, stream=stream)
 
-    with torch.cuda.stream(stream):
-        phase(B.PHASE_TOKEN_SCALES | B.PHASE_GEMM1 | B.PHASE_GEMM2)
+        def phase(ph):
+            B.moe_expert_forward(xq, xs, qe.w1q, qe.w1s, qe.w2q, qe.w2s, idx, wts, counts, offsets, perm, y_pairs,
+                                 ews, tile_n=args.tile_n, phases=ph, stream=stream)
+
+        with torch.cuda.stream(stream):
+            phase(B.PHASE_TOKEN_SCALES | B.PHASE_GEMM1 | B.PHASE_GEMM2)
     stream.synchronize()
     if args.launch_list:
         # after the forward replays: one launch of each GEMM phase alone (the
@@ -311,7 +369,7 @@ def run_ours(args, rank, world, local_rank):
     assert B.moe_get_device_status(ews, stream) == 0
     g1_ms, g2_ms = statistics.mean(g1), statistics.mean(g2)
 
-    alg = algorithmic(wl, counts_np)
+    alg = algorithmic_bfp8(wl, counts_np) if bfp8 else algorithmic(wl, counts_np)
     hbm, bf16, peak_src = peaks()
     fp8_peak_tflops = 2 * bf16                      # FP8 dense = 2x BF16 dense (nominal ratio)
     dom = "gemm1" if g1_ms >= g2_ms else "gemm2"
@@ -328,16 +386,20 @@ def run_ours(args, rank, world, local_rank):
         achieved = dom_flops / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": fp8_peak_tflops, "unit": "TFLOP/s",
                 "frac": round(achieved / fp8_peak_tflops, 4)}
-    roof.update({"kernel": f"expert_gemm_kernel ({dom}, one launch)", "ms": round(dom_ms, 5),
+    kname = "bfp8_gemm_kernel" if bfp8 else "expert_gemm_kernel"
+    roof.update({"kernel": f"{kname} ({dom}, one launch)", "ms": round(dom_ms, 5),
                  "algorithmic_bytes": dom_bytes, "algorithmic_flops": dom_flops,
-                 "traffic": measured_traffic(wl.name, dom), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)"})
+                 "traffic": measured_traffic(wl.name, dom, bfp8), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)"})
     layer_time_bound = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (fp8_peak_tflops * 1e12))
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic (seeded, workloads/)",
-        "config": {"workload": wl.describe(), "tokens_per_step": T, "pairs": T * k,
+        "vs_baseline": None,
+        "dtype": "fp8xfp8, 128x128 block scales (fp32 accumulate)" if bfp8 else "fp8xfp4 (fp32 accumulate)",
+        "data": "synthetic (seeded, workloads/)",
+        "config": {"workload": wl.describe() + (" block-FP8 weights" if bfp8 else ""), "tokens_per_step": T,
+                   "pairs": T * k, "weights": args.weights + (" (tile-contiguous codes)" if bfp8 else ""),
                    "touched_experts": alg["touched_experts"], "tile_n": args.tile_n or "auto",
                    "l2": "flushed between steps (512 MiB write + 512 MiB read)" if not args.no_flush else "not flushed",
                    "cuda_graph": True, "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -371,59 +433,69 @@ def run_ours(args, rank, world, local_rank):
                          "h2d_bytes_per_step": x_h.numel() * 2 + l_h.numel() * 4,
                          "d2h_bytes_per_step": y_h.numel() * 2}
         if rank == 0 and world == 1:
-            result["cpu_baseline"] = cpu_baseline(wl, steps=2)
+            result["cpu_baseline"] = cpu_baseline(wl, steps=2, bfp8=bfp8)
     return result
 
 
 # ---------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(wl, n_tokens=2):
+def _oracle_sample(wl, n_tokens=2, bfp8=False):
     """A fixed token sample of the workload and the oracle-quantised experts it needs."""
     import numpy as np
     import torch
 
     import workloads as W
+    from oracle import bfp8 as OB
     from oracle import moe as O
     x, logits = W.tokens(wl)
     idx, _ = O.route_topk(logits[:n_tokens].numpy(), wl.k)
     need = sorted(set(idx.reshape(-1).tolist()))
     E, H, I = wl.E, wl.H, wl.I
-    w1q = np.zeros((E, 2 * I, H // 2), np.uint8); w1s = np.zeros((E, 2 * I, H // 32), np.uint8)
-    w2q = np.zeros((E, H, I // 2), np.uint8); w2s = np.zeros((E, H, I // 32), np.uint8)
+    if bfp8:
+        quant = OB.quantize_weight
+        w1q = np.zeros((E, 2 * I, H), np.uint8); w1s = np.zeros((E, 2 * I // 128, H // 128), np.float32)
+        w2q = np.zeros((E, H, I), np.uint8); w2s = np.zeros((E, H // 128, I // 128), np.float32)
+    else:
+        quant = O.quantize_weight
+        w1q = np.zeros((E, 2 * I, H // 2), np.uint8); w1s = np.zeros((E, 2 * I, H // 32), np.uint8)
+        w2q = np.zeros((E, H, I // 2), np.uint8); w2s = np.zeros((E, H, I // 32), np.uint8)
     for e in need:
         l1, l2 = W.expert_weights(wl, e, "cpu")
-        q, s = O.quantize_weight(l1.view(torch.int16).numpy().view(np.uint16)[None])
+        q, s = quant(l1.view(torch.int16).numpy().view(np.uint16)[None])
         w1q[e], w1s[e] = q[0], s[0]
-        q, s = O.quantize_weight(l2.view(torch.int16).numpy().view(np.uint16)[None])
+        q, s = quant(l2.view(torch.int16).numpy().view(np.uint16)[None])
         w2q[e], w2s[e] = q[0], s[0]
     xb = x[:n_tokens].view(torch.int16).numpy().view(np.uint16)
-    return xb, logits[:n_tokens].numpy(), (w1q, w1s, w2q, w2s)
+    return xb, logits[:n_tokens].numpy(), (w1q, w1s, w2q, w2s), bfp8
 
 
 def _oracle_step(wl, sample):
+    from oracle import bfp8 as OB
     from oracle import moe as O
-    xb, lg, w = sample
-    O.forward(xb, lg, *w, wl.k)
+    xb, lg, w, bfp8 = sample
+    (OB if bfp8 else O).forward(xb, lg, *w, wl.k)
 
 
-def cpu_baseline(wl, steps=2, n_tokens=2):
-    sample = _oracle_sample(wl, n_tokens)
+def cpu_baseline(wl, steps=2, n_tokens=2, bfp8=False):
+    sample = _oracle_sample(wl, n_tokens, bfp8)
     _oracle_step(wl, sample)
     t0 = time.time()
     for _ in range(steps):
         _oracle_step(wl, sample)
     dt = (time.time() - t0) / steps
+    what = "block-FP8 oracle" if bfp8 else "oracle"
     return {"value": round(n_tokens / dt, 3), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
             "sample": f"{n_tokens} tokens of {wl.describe()} ({n_tokens * wl.k} pairs) per step, float64 "
-                      f"NumPy oracle (weights of the experts they route to quantised untimed), {steps} steps"}
+                      f"NumPy {what} (weights of the experts they route to quantised untimed), {steps} steps"}
 
 
 def run_reference(args):
     import workloads as W
     wl = W.WORKLOADS[args.workload]
     n_tokens = 2
-    sample = _oracle_sample(wl, n_tokens)
+    bfp8 = args.weights == "bfp8"
+    sample = _oracle_sample(wl, n_tokens, bfp8)
     for _ in range(args.warmup):
         _oracle_step(wl, sample)
     times = []
@@ -435,12 +507,13 @@ def run_reference(args):
     value = n_tokens * args.steps / total
     cores = len(os.sched_getaffinity(0))
     sample_txt = (f"{n_tokens} tokens of {wl.describe()} ({n_tokens * wl.k} pairs) per step, float64 NumPy "
-                  f"oracle, weights of the routed experts quantised untimed")
+                  f"{'block-FP8 ' if bfp8 else ''}oracle, weights of the routed experts quantised untimed")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded, workloads/)", "config": {"workload": wl.describe(),
-                                                                  "tokens_per_step": n_tokens},
+            "data": "synthetic (seeded, workloads/)",
+            "config": {"workload": wl.describe() + (" block-FP8 weights" if bfp8 else ""),
+                       "tokens_per_step": n_tokens, "weights": args.weights},
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample_txt},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -458,6 +531,17 @@ def launches_per_forward(T, H, E, k):
     if P * H <= (16 << 20):
         return 1 + permute + 1 + 3             # route, permute, pool cast, GEMM1, GEMM2, combine
     return 1 + 1 + permute + 1 + 3             # quant, route, permute, pool prep, GEMM1, GEMM2, combine
+
+
+def launches_per_forward_bfp8(T, H, E, k):
+    """Kernels one moe_forward_bfp8 launches (csrc/bfp8.cu): small problems the
+    front (routing + permute + pool cast) and one launch of GEMM1 + GEMM2 +
+    combine; otherwise routing, permute, pool cast, GEMM1, GEMM2, combine."""
+    P = T * k
+    if 1 <= T <= 64 and E <= 256 and P * H <= (4 << 20):
+        return 2
+    permute = 1 if P <= 2048 else 2
+    return 1 + permute + 1 + 3
 
 
 def main():

@@ -24,9 +24,15 @@
  *     round-to-nearest-even of value / scale computed in float32, saturating
  *     at +-448; the sign of values that round to zero is kept.  A group whose
  *     amax is 0 has scale 0 and all codes 0.
- *   - Weights are in the natural layout: l1 codes [E][2I][H] (gate rows
- *     [0,I), up rows [I,2I)), scales [E][2I/128][H/128]; l2 codes [E][H][I],
- *     scales [E][H/128][I/128].
+ *   - Weights: l1 [E][2I][H] (gate rows [0,I), up rows [I,2I)) with scales
+ *     [E][2I/128][H/128]; l2 [E][H][I] with scales [E][H/128][I/128].  The
+ *     scales are always in that order; the codes are stored in one of two
+ *     layouts (enum bfp8_layout):
+ *       BFP8_LAYOUT_CANONICAL: row-major [G][N][K];
+ *       BFP8_LAYOUT_TILED: tile-contiguous [G][N/128][K/128][128][128] --
+ *         each 128 x 128 block is 16 KB in one piece (rows of 128 codes), so
+ *         that a GEMM streams whole DRAM pages instead of 128-byte pieces of
+ *         rows 2 KB apart.
  *
  * Conventions are those of moe_mxq.h: device pointers owned by the caller,
  * no allocation, no synchronisation, work enqueued on `stream`, a moe_status
@@ -53,11 +59,14 @@ extern "C" {
 MOE_API int bfp8_quantize_act(const uint16_t *x, int64_t rows, int64_t K, uint8_t *q, float *s,
                               cudaStream_t stream);
 
-/* BF16 [G, N, K] -> E4M3 codes [G, N, K] (natural row-major layout) and
- * float32 scales [G, N/128, K/128], one per 128 x 128 block (MonoMoe kernel
- * design, "Fixed shape").  N and K must be multiples of 128. */
-MOE_API int bfp8_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int64_t K, uint8_t *q, float *s,
-                                 cudaStream_t stream);
+enum bfp8_layout { BFP8_LAYOUT_CANONICAL = 0, BFP8_LAYOUT_TILED = 1 };
+
+/* BF16 [G, N, K] -> E4M3 codes (layout: enum bfp8_layout) and float32 scales
+ * [G, N/128, K/128], one per 128 x 128 block (MonoMoe kernel design, "Fixed
+ * shape").  N and K must be multiples of 128; another layout value:
+ * MOE_ERR_INVALID_ARG. */
+MOE_API int bfp8_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int64_t K, int layout, uint8_t *q,
+                                 float *s, cudaStream_t stream);
 
 typedef struct moe_bfp8_args {
     uint32_t struct_size;      /* sizeof(moe_bfp8_args) */
@@ -82,6 +91,13 @@ typedef struct moe_bfp8_args {
     float *hs_out;             /* [T*k, I/128] */
     void *workspace;           /* moe_bfp8_workspace_size bytes, 256-byte aligned */
     size_t workspace_bytes;
+    int32_t weight_layout;     /* enum bfp8_layout of w1q and w2q */
+    /* 0: the whole layer.  MOE_PHASE_GEMM1 and/or MOE_PHASE_GEMM2: only those
+     * GEMM launches, on the routing, permute, pool rows and h that an earlier
+     * whole-layer call with the same arguments left in the workspace (and in
+     * the optional outputs); y and the routing are not touched.  Used to time
+     * one GEMM.  Other bits: MOE_ERR_INVALID_ARG. */
+    int32_t phases;
 } moe_bfp8_args;
 
 /* Workspace bytes moe_forward_bfp8 needs for this shape (0 for invalid sizes). */

@@ -41,6 +41,7 @@ MOE_ERR_DEVICE_INDEX = 7
 LAYOUT_CANONICAL, LAYOUT_MMA_L1, LAYOUT_MMA_L2 = 0, 1, 2
 PHASE_TOKEN_SCALES, PHASE_GEMM1, PHASE_GEMM2, PHASE_H_SCALES = 1, 2, 4, 8
 ROUTE_SOFTMAX, ROUTE_SIGMOID, ROUTE_RAW, ROUTE_NO_RENORM = 0, 1, 2, 4
+BFP8_LAYOUT_CANONICAL, BFP8_LAYOUT_TILED = 0, 1
 
 EXPORTED = ["mxq_quantize_act", "mxq_quantize_weight", "moe_route_topk", "moe_route_topk_ex",
             "moe_permute_workspace_size",
@@ -83,7 +84,7 @@ class MoeBfp8Args(ctypes.Structure):
                 ("x", _p), ("logits", _p), ("w1q", _p), ("w1s", _p), ("w2q", _p), ("w2s", _p), ("y", _p),
                 ("topk_idx_out", _p), ("topk_w_out", _p), ("counts_out", _p), ("offsets_out", _p),
                 ("perm_out", _p), ("hq_out", _p), ("hs_out", _p),
-                ("workspace", _p), ("workspace_bytes", _sz)]
+                ("workspace", _p), ("workspace_bytes", _sz), ("weight_layout", _i32), ("phases", _i32)]
 
 
 lib.mxq_quantize_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
@@ -102,7 +103,7 @@ lib.moe_workspace_size.argtypes = [_i64, _i64, _i64, _i32, _i32]
 lib.moe_workspace_size.restype = _sz
 lib.moe_forward.argtypes = [ctypes.POINTER(MoeForwardArgs), _p]
 lib.bfp8_quantize_act.argtypes = [_p, _i64, _i64, _p, _p, _p]
-lib.bfp8_quantize_weight.argtypes = [_p, _i64, _i64, _i64, _p, _p, _p]
+lib.bfp8_quantize_weight.argtypes = [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p, _p]
 lib.moe_bfp8_workspace_size.argtypes = [_i64, _i64, _i64, _i32, _i32]
 lib.moe_bfp8_workspace_size.restype = _sz
 lib.moe_forward_bfp8.argtypes = [ctypes.POINTER(MoeBfp8Args), _p]
@@ -273,10 +274,11 @@ def bfp8_quantize_act(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=
     return rc
 
 
-def bfp8_quantize_weight(w: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None, check=True) -> int:
-    """w bf16 [G, N, K] -> q uint8 [G, N, K] (E4M3), s float32 [G, N/128, K/128]."""
+def bfp8_quantize_weight(w: torch.Tensor, q: torch.Tensor, s: torch.Tensor, layout: int = BFP8_LAYOUT_TILED,
+                         stream=None, check=True) -> int:
+    """w bf16 [G, N, K] -> q uint8 (E4M3, G*N*K codes in ``layout``), s float32 [G, N/128, K/128]."""
     G, N, K = w.shape
-    rc = lib.bfp8_quantize_weight(_ptr(w), G, N, K, _ptr(q), _ptr(s), _stream(stream))
+    rc = lib.bfp8_quantize_weight(_ptr(w), G, N, K, layout, _ptr(q), _ptr(s), _stream(stream))
     if check:
         _check(rc, "bfp8_quantize_weight")
     return rc
@@ -288,14 +290,16 @@ def moe_bfp8_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
 
 def moe_forward_bfp8(x, logits, w1q, w1s, w2q, w2s, k: int, y, workspace, topk_idx_out=None, topk_w_out=None,
                      counts_out=None, offsets_out=None, perm_out=None, hq_out=None, hs_out=None,
-                     route_mode: int = ROUTE_SOFTMAX, stream=None, check=True) -> int:
+                     route_mode: int = ROUTE_SOFTMAX, phases: int = 0, weight_layout: int = BFP8_LAYOUT_TILED,
+                     stream=None, check=True) -> int:
     T, H = x.shape
     E = logits.shape[1]
-    I = w2q.shape[2]
+    I = w2s.shape[2] * 128
     a = MoeBfp8Args(ctypes.sizeof(MoeBfp8Args), T, H, I, E, k, route_mode,
                     _ptr(x), _ptr(logits), _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s), _ptr(y),
                     _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), _ptr(offsets_out), _ptr(perm_out),
-                    _ptr(hq_out), _ptr(hs_out), _ptr(workspace), workspace.numel() * workspace.element_size())
+                    _ptr(hq_out), _ptr(hs_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                    weight_layout, phases)
     rc = lib.moe_forward_bfp8(ctypes.byref(a), _stream(stream))
     if check:
         _check(rc, "moe_forward_bfp8")

@@ -27,6 +27,8 @@
 // rows y_pair[slot][token], which the combine sums in slot order.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "../../include/moe_bfp8.h"
 #include "host_common.h"
 #include "layer_blocks.cuh"
@@ -97,10 +99,11 @@ __global__ void __launch_bounds__(kCastThreads) bfp8_cast_kernel(const uint4 *__
 }
 
 // Weight cast: one CTA per 128 x 128 block (grid-stride), 256 threads, each
-// thread 64 values of one row (half a block row).
+// thread 64 values of one row (half a block row).  Codes row-major, or
+// tile-contiguous (tiled: block b's 16 KB at b * 16 KB, rows of 128 codes).
 constexpr int kWqThreads = 256;
 __global__ void __launch_bounds__(kWqThreads) bfp8_weight_kernel(const uint4 *__restrict__ w, int64_t G, int64_t N,
-                                                                 int64_t K, uint4 *__restrict__ q,
+                                                                 int64_t K, int tiled, uint4 *__restrict__ q,
                                                                  float *__restrict__ s) {
   pdl_launch_dependents();
   pdl_wait();
@@ -147,41 +150,110 @@ __global__ void __launch_bounds__(kWqThreads) bfp8_weight_kernel(const uint4 *__
       out.y = e4m3x4_scaled(f[4], f[5], f[6], f[7], sc);
       out.z = e4m3x4_scaled(h[0], h[1], h[2], h[3], sc);
       out.w = e4m3x4_scaled(h[4], h[5], h[6], h[7], sc);
-      q[elem0 / 16 + i] = out;
+      const int64_t dst = tiled ? (b * 16384 + r * 128 + half * 64) / 16 : elem0 / 16;
+      q[dst + i] = out;
     }
     __syncthreads();                      // warp_max / block_scale reused by the next block
   }
 }
 
-// y[t] = bf16( sum over valid slots j, in slot order, of y_pairs[j][t] ) with
-// a float32 sum; the pairs' rows already carry their top-k weight.  One
-// thread per 8 output values.
-__global__ void __launch_bounds__(kCastThreads) bfp8_combine_kernel(const float4 *__restrict__ y_pairs,
-                                                                    const int32_t *__restrict__ idx, int64_t T,
-                                                                    int k, int64_t H, uint4 *__restrict__ y) {
+// Small problems (T <= 64, E <= 256): routing, the counting-sort permute and
+// the pool cast in one launch.  One CTA per 128-column group of x: every CTA
+// routes all tokens (one warp per token) and ranks all pairs -- the same
+// result in every CTA, CTA 0 writes the routing and permute outputs -- then
+// casts its column group of every pool row (16 threads per row).
+constexpr int kBFrontThreads = 256;
+constexpr int kBFrontMaxT = 64, kBFrontMaxE = 256;
+
+__global__ void __launch_bounds__(kBFrontThreads) bfp8_front_kernel(
+    const float *__restrict__ logits, const uint4 *__restrict__ x, int T, int E, int k, int H, int mode,
+    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts_out,
+    int32_t *__restrict__ offsets_out, int32_t *__restrict__ perm_out, uint2 *__restrict__ xq,
+    float *__restrict__ xs) {
+  constexpr int kW = kBFrontThreads / 32;
+  extern __shared__ __align__(16) unsigned char fsm[];
+  const int P = T * k, g = blockIdx.x, KB = H / 128, H8 = H / 8;
+  uint4 *xsm = reinterpret_cast<uint4 *>(fsm);                          // [T][16]: this CTA's columns
+  int *idx_sm = reinterpret_cast<int *>(xsm + (size_t)T * 16);          // [P]
+  int *perm_sm = idx_sm + P;                                            // [P]
+  int *cnt = perm_sm + P;                                               // [E + 1]
+  int *base = cnt + (E + 1);                                            // [E]
+  int *warp_sums = base + E;                                            // [kW]
+  int *total = warp_sums + kW;                                          // [1]
+  uint16_t *wc = reinterpret_cast<uint16_t *>(total + 4);               // [kW][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool writer = blockIdx.x == 0;
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t H8 = H / 8;
-  const int64_t items = T * H8;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t t = i / H8, c = i - t * H8;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      if (__ldg(idx + t * k + j) < 0) continue;
-      const float4 *row = y_pairs + (((int64_t)j * T + t) * H) / 4 + 2 * c;
-      const float4 a = __ldg(row), b = __ldg(row + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  // 0. this CTA's 128 columns of every token; the first 16 bytes per thread
+  // wait in a register while the logits load
+  const int nx = T * 16;
+  uint4 xv = make_uint4(0, 0, 0, 0);
+  if (tid < nx) xv = __ldg(x + (size_t)(tid >> 4) * H8 + g * 16 + (tid & 15));
+  for (int i = tid + kBFrontThreads; i < nx; i += kBFrontThreads)
+    xsm[i] = __ldg(x + (size_t)(i >> 4) * H8 + g * 16 + (i & 15));
+  // 1. routing, one warp per token
+  for (int t = warp; t < T; t += kW) {
+    int my_idx;
+    float my_w;
+    warp_route_token<kBFrontMaxE / 32>(logits + (size_t)t * E, E, k, lane, mode, &my_idx, &my_w);
+    if (lane < k) {
+      idx_sm[t * k + lane] = my_idx;
+      if (writer) {
+        idx_out[t * k + lane] = my_idx;
+        w_out[t * k + lane] = my_w;
+      }
     }
-    uint32_t packed[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * p]));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * p + 1]));
-      packed[p] = lo | (hi << 16);
-    }
-    y[i] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    __syncwarp();
   }
+  if (tid < nx) xsm[tid] = xv;
+  for (int e = tid; e <= E; e += kBFrontThreads) cnt[e] = 0;
+  __syncthreads();
+  // 2. count -> exclusive prefix -> stable ranks
+  for (int p = tid; p < P; p += kBFrontThreads) atomicAdd(&cnt[idx_sm[p]], 1);
+  __syncthreads();
+  const int o = block_exclusive_scan<kBFrontThreads>(tid < E ? cnt[tid] : 0, warp_sums, total);
+  if (tid < E) {
+    base[tid] = o;
+    if (writer) {
+      counts_out[tid] = cnt[tid];
+      offsets_out[tid] = o;
+    }
+  }
+  if (tid == 0 && writer) offsets_out[E] = *total;
+  __syncthreads();
+  block_stable_ranks<kBFrontThreads>([&](int64_t p) { return idx_sm[p]; }, 0, P, E, base, wc,
+                                     writer ? perm_out : nullptr, nullptr, perm_sm);
+  // 3. this CTA's 128-value group of every pool row
+  for (int b0 = 0; b0 < P * 16; b0 += kBFrontThreads) {
+    const int i = b0 + tid;
+    const bool valid = i < P * 16;      // P * 16 is a multiple of 16: 16-lane groups stay whole
+    const int sr = i >> 4, sub = i & 15;
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid) unpack_bf16x8(xsm[(perm_sm[sr] / k) * 16 + sub], f);
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    if (!valid) continue;
+    const float sc = __fdiv_rn(amax, kE4M3Max);
+    uint2 out;
+    out.x = e4m3x4_scaled(f[0], f[1], f[2], f[3], sc);
+    out.y = e4m3x4_scaled(f[4], f[5], f[6], f[7], sc);
+    xq[(size_t)sr * H8 + g * 16 + sub] = out;
+    if (sub == 0) xs[(size_t)sr * KB + g] = sc;
+  }
+}
+
+size_t bfp8_front_smem(int T, int E, int k) {
+  const int P = T * k;
+  return (size_t)T * 256 + (size_t)2 * P * 4 + (size_t)(2 * E + 1) * 4 + (kBFrontThreads / 32) * 4 + 16 +
+         (size_t)(kBFrontThreads / 32) * E * 2;
+}
+
+bool bfp8_front_eligible(int64_t T, int64_t H, int E, int k) {
+  return T >= 1 && T <= kBFrontMaxT && E <= kBFrontMaxE && T * k * H <= (int64_t(4) << 20);
 }
 
 // ---------------------------------------------------------------- expert GEMMs
@@ -208,11 +280,17 @@ constexpr int kGOffSc = kGOffScan + 64;               // scales: weights [2][KB]
 static_assert(kGNumBars * 8 <= 256, "barrier area");
 static_assert(kGTmemCols * kGCtasPerSm <= 512, "co-resident CTAs share the SM's TMEM");
 
+// PHASE 1: GEMM1 (+ SiLU(gate) * up + FP8 write-back of h); 2: GEMM2 (+ the
+// top-k weight, FP32 pair rows); 3: both and the combine in one launch (small
+// problems, every CTA resident): GEMM1 items first, then GEMM2 items, each
+// waiting on the arrival counter of its token tile that the GEMM1 epilogues
+// raise, then the combine, after the counter of finished GEMM2 items -- the
+// pages' arrival mask between the two GEMMs, as bounded waits.
 template <int PHASE>
 struct GCfg {
-  static constexpr int kHalves = PHASE == 1 ? 2 : 1;           // weight tiles per K block
-  static constexpr int kSlotCols = kHalves * kGBN;             // TMEM columns of one K block's partial
-  static constexpr int kSlots = (int)kGTmemCols / kSlotCols;   // 4 (GEMM1) or 8 (GEMM2)
+  // TMEM columns of one K block's partial: gate and up halves for GEMM1 items
+  static constexpr int kSlotCols = PHASE == 2 ? kGBN : 2 * kGBN;
+  static constexpr int kSlots = (int)kGTmemCols / kSlotCols;   // 4 (GEMM1 items) or 8
 };
 
 __host__ __device__ inline size_t gemm_sc_bytes(int KB) { return ((size_t)KB * (2 + kGBN) * 4 + 15) / 16 * 16; }
@@ -222,17 +300,23 @@ inline size_t gemm_smem_bytes(int KB, int E) {
 
 struct BGemmArgs {
   int E, k, T, H, I;
-  int KB;                          // K blocks (H/128 for GEMM1, I/128 for GEMM2)
-  int MT;                          // 128-row output tiles per expert (I/128 for GEMM1, H/128 for GEMM2)
+  int KB, MT;                      // the launch's (first) GEMM: K blocks, 128-row output tiles per expert
+  int KB2, MT2;                    // PHASE 3: GEMM2's
   int P;                           // pool rows (T * k, dropped pairs excluded from the tiles)
+  int tiled;                       // weight codes tile-contiguous (else row-major)
   const int32_t *counts, *offsets, *perm;
   const float *topk_w;             // [T*k] by pair id
   const float *w_scales;           // GEMM1: [E][2I/128][KB]; GEMM2: [E][H/128][KB]
   const float *x_scales;           // token scales of the pool rows [P][KB]
+  const float *w_scales2;          // PHASE 3: GEMM2's weight-block scales
+  const float *x_scales2;          // PHASE 3: hs
   uint8_t *hq;                     // GEMM1 out [P][I]
   float *hs;                       // GEMM1 out [P][I/128]
   float *y_pairs;                  // GEMM2 out [k][T][H]
   int *status;
+  int *sync;                       // PHASE 3: [0] GEMM2 items done, [1 + g] GEMM1 items of token tile g done
+  const int32_t *topk_idx;         // PHASE 3: combine (dropped slots skipped)
+  uint4 *y;                        // PHASE 3: combine output [T][H] bf16
 };
 
 __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -259,11 +343,11 @@ __device__ __forceinline__ uint32_t idesc_e4m3_f32(uint32_t n) {
 }
 
 struct BTile {
-  int e, mt, s0, valid;
+  int e, mt, g, s0, valid;         // expert, output tile, global token tile, first pool row, valid tokens
 };
 
-// Work item w -> (expert, output tile, first pool row, valid tokens); items
-// are expert-major, then output tile, then token tile.
+// Work item w -> its tile; items are expert-major, then output tile, then
+// token tile.
 __device__ __forceinline__ BTile decode_item(int w, int MT, int E, const int *tile_off, const int *cnt,
                                              const int *off) {
   const int tq = w / MT;
@@ -278,17 +362,78 @@ __device__ __forceinline__ BTile decode_item(int w, int MT, int E, const int *ti
   const int local = w - tile_off[lo] * MT;
   ti.mt = local / nte;
   const int nt = local - ti.mt * nte;
+  ti.g = tile_off[lo] + nt;
   ti.s0 = off[lo] + nt * kGBN;
   const int rem = cnt[lo] - nt * kGBN;
   ti.valid = rem < kGBN ? rem : kGBN;
   return ti;
 }
 
+// Output items [first, n) step `stride` of the combine: y[t] (8 values per
+// item) = bf16( sum over valid slots j, in slot order, of y_pairs[j][t] ).
+// from_l2: the pair rows were written by other CTAs of the same launch.
+__device__ __forceinline__ void combine_items(int64_t first, int64_t stride, const float4 *y_pairs,
+                                              const int32_t *idx, int64_t T, int k, int64_t H, uint4 *y,
+                                              bool from_l2) {
+  const int64_t H8 = H / 8;
+  for (int64_t i = first; i < T * H8; i += stride) {
+    const int64_t t = i / H8, c = i - t * H8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      if (__ldg(idx + t * k + j) < 0) continue;
+      const float4 *row = y_pairs + (((int64_t)j * T + t) * H) / 4 + 2 * c;
+      const float4 a = from_l2 ? __ldcg(row) : __ldg(row);
+      const float4 b = from_l2 ? __ldcg(row + 1) : __ldg(row + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    uint32_t packed[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * p]));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * p + 1]));
+      packed[p] = lo | (hi << 16);
+    }
+    y[i] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
+// The combine as its own launch (larger problems): the pairs' rows already
+// carry their top-k weight.
+__global__ void __launch_bounds__(kCastThreads) bfp8_combine_kernel(const float4 *__restrict__ y_pairs,
+                                                                    const int32_t *__restrict__ idx, int64_t T,
+                                                                    int k, int64_t H, uint4 *__restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
+  combine_items((int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x, y_pairs, idx, T,
+                k, H, y, false);
+}
+
+// Optional wait-time accounting (build with -DMOE_MXQ_WAIT_STATS): each role
+// adds the clock cycles it spent in bounded waits, and its total, to 64-bit
+// counters at byte 64 of the status area: [0] producer on empty stages,
+// [1] MMA on full stages, [2] MMA on free TMEM slots, [3] epilogue on full
+// slots, [4] kernel cycles of warp 0, [5] of warp 1, [6] of warp 2, [7] work
+// items.
+#ifdef MOE_MXQ_WAIT_STATS
+#define BFP8_TIMED_WAIT(slot, expr)                                  \
+  ([&]() {                                                           \
+    const long long _t0 = clock64();                                 \
+    const bool _r = (expr);                                          \
+    if (lane == 0) wait_acc[slot] += clock64() - _t0;                \
+    return _r;                                                       \
+  }())
+#else
+#define BFP8_TIMED_WAIT(slot, expr) (expr)
+#endif
+
 template <int PHASE>
 __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
     bfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_b2,
                      const BGemmArgs args) {
   using C = GCfg<PHASE>;
+  constexpr bool kFused = PHASE == 3;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
@@ -299,24 +444,34 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
   uint64_t *slot_empty = slot_full + 8;
   uint64_t *mma_done = slot_empty + 8;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + kGOffMisc);
+  int *flag = reinterpret_cast<int *>(smem + kGOffMisc + 8);            // combine go-ahead
   int *vote = reinterpret_cast<int *>(smem + kGOffMisc + 16);           // [4]
   float *colmax = reinterpret_cast<float *>(smem + kGOffMisc + 64);     // [4][16]
   int *row_pair = reinterpret_cast<int *>(smem + kGOffMisc + 320);      // [16]
   float *row_w = reinterpret_cast<float *>(smem + kGOffMisc + 384);     // [16]
   int *scan_ws = reinterpret_cast<int *>(smem + kGOffScan);
-  float *sw = reinterpret_cast<float *>(smem + kGOffSc);                // [kHalves][KB]
-  float *sx = sw + 2 * args.KB;                                         // [KB][16]
-  int *tile_off = reinterpret_cast<int *>(smem + kGOffSc + gemm_sc_bytes(args.KB));
+  const int kb_max = kFused ? max(args.KB, args.KB2) : args.KB;
+  float *sw = reinterpret_cast<float *>(smem + kGOffSc);                // [halves][KB]
+  float *sx = sw + 2 * kb_max;                                          // [KB][16]
+  int *tile_off = reinterpret_cast<int *>(smem + kGOffSc + gemm_sc_bytes(kb_max));
   int *cnt_sm = tile_off + (args.E + 1);
   int *off_sm = cnt_sm + (args.E + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int *status = args.status;
+#ifdef MOE_MXQ_WAIT_STATS
+  long long wait_acc[4] = {0, 0, 0, 0};
+  const long long k_t0 = clock64();
+#endif
 
   pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
       tma_prefetch_desc(&tmap_b);
+      if (kFused) {
+        tma_prefetch_desc(&tmap_w2);
+        tma_prefetch_desc(&tmap_b2);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -347,35 +502,103 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_ptr;
-  const int total = tile_off[args.E] * args.MT;
-  const int KB = args.KB;
+  const int n1 = tile_off[args.E] * args.MT;
+  const int n2 = kFused ? tile_off[args.E] * args.MT2 : 0;
+  const int total = n1 + n2;
+  struct Item {
+    BTile ti;
+    bool l1, second;                 // a GEMM1 item; the single launch's GEMM2 item
+    int KB, MT, halves;
+  };
+  auto get_item = [&](int w) {
+    Item it;
+    it.second = kFused && w >= n1;
+    it.l1 = PHASE == 1 || (kFused && !it.second);
+    it.KB = it.second ? args.KB2 : args.KB;
+    it.MT = it.second ? args.MT2 : args.MT;
+    it.halves = it.l1 ? 2 : 1;
+    it.ti = decode_item(it.second ? w - n1 : w, it.MT, args.E, tile_off, cnt_sm, off_sm);
+    return it;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int stage = 0;
     uint32_t phase = 0, issued_mask = 0, issued_phase = 0;
     bool ok = true;
+    auto record = [&](int st, uint32_t ph) {
+      issued_mask |= 1u << st;
+      issued_phase = (issued_phase & ~(1u << st)) | (ph << st);
+    };
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      const BTile ti = decode_item(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
-      // weight rows of this item's tile(s) in the [E * rows][K] tensor map
-      const int rows_per_expert = PHASE == 1 ? 2 * args.I : args.H;
-      const int row0 = ti.e * rows_per_expert + ti.mt * 128;
-      for (int kb = 0; kb < KB && ok; ++kb) {
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1, status, kGWaitLimit, kWaitProducerEmpty, kb))) {
-            ok = false;
+      const Item it = get_item(w);
+      const CUtensorMap *tw = it.second ? &tmap_w2 : &tmap_w;
+      const CUtensorMap *tb = it.second ? &tmap_b2 : &tmap_b;
+      // weight rows of this item's tile(s) in the [E * rows][K] weight tensor
+      const int row0 = it.ti.e * (it.l1 ? 2 * args.I : args.H) + it.ti.mt * 128;
+      const int nst = it.KB * it.halves;                    // stages of this item
+      // stage a: K block a / halves, half (gate, up) a % halves; row-major codes:
+      // the box at (K offset, row); tiled: block (row / 128, kb) is rows
+      // [(row / 128 * KB + kb) * 128, +128) of a 128-byte-wide tensor
+      auto issue_w = [&](int st, int a) {
+        const int kb = a / it.halves, wrow = row0 + (a - kb * it.halves) * args.I;
+        mbar_arrive_expect_tx(&full[st], (uint32_t)(kGTileA + kGTileB));
+        if (args.tiled)
+          tma_load_2d(smem + kGOffA + st * kGTileA, tw, &full[st], 0, ((wrow >> 7) * it.KB + kb) * 128);
+        else
+          tma_load_2d(smem + kGOffA + st * kGTileA, tw, &full[st], kb * 128, wrow);
+      };
+      auto issue_b = [&](int st, int a) {
+        tma_load_2d(smem + kGOffB + st * kGTileB, tb, &full[st], (a / it.halves) * 128, it.ti.s0);
+      };
+      int a0 = 0;
+      if (it.second) {
+        // the weight parts of the first stages now, then the wait for the h
+        // rows of the token tile (all its GEMM1 items), then their token
+        // parts -- issued even after a failed wait, so that every armed
+        // barrier completes (the status word says why)
+        const int npre = min(nst, kGStages);
+        const int st0 = stage;
+        const uint32_t ph0 = phase;
+        int armed = 0;
+        for (; armed < npre; ++armed) {
+          if (!__all_sync(0xffffffffu, BFP8_TIMED_WAIT(0, mbar_wait(&empty[stage], phase ^ 1, status, kGWaitLimit, kWaitProducerEmpty, armed))))
             break;
-          }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&full[stage], (uint32_t)(kGTileA + kGTileB));
-            tma_load_2d(smem + kGOffA + stage * kGTileA, &tmap_w, &full[stage], kb * 128, row0 + hf * args.I);
-            tma_load_2d(smem + kGOffB + stage * kGTileB, &tmap_b, &full[stage], kb * 128, ti.s0);
-          }
+          if (lane == 0) issue_w(stage, armed);
           __syncwarp();
-          issued_mask |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == kGStages) { stage = 0; phase ^= 1; }
         }
+        bool dep_ok = true;
+        if (lane == 0) {
+          dep_ok = wait_counter(args.sync + 1 + it.ti.g, args.MT, status, kGWaitLimit, w);
+          fence_proxy_async_global();
+        }
+        dep_ok = __shfl_sync(0xffffffffu, dep_ok ? 1 : 0, 0) != 0;
+        for (int a = 0; a < armed; ++a) {
+          // armed <= kGStages: the ring wraps at most once inside one item
+          const int st = (st0 + a) % kGStages;
+          if (lane == 0) issue_b(st, a);
+          record(st, ph0 ^ (uint32_t)((st0 + a) / kGStages));
+        }
+        __syncwarp();
+        if (armed < npre || !dep_ok) {
+          ok = false;
+          break;
+        }
+        a0 = npre;
+      }
+      for (int a = a0; a < nst; ++a) {
+        if (!__all_sync(0xffffffffu, BFP8_TIMED_WAIT(0, mbar_wait(&empty[stage], phase ^ 1, status, kGWaitLimit, kWaitProducerEmpty, a)))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          issue_w(stage, a);
+          issue_b(stage, a);
+        }
+        __syncwarp();
+        record(stage, phase);
+        if (++stage == kGStages) { stage = 0; phase ^= 1; }
       }
     }
     // never leave with copies in flight
@@ -389,14 +612,15 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
     bool ok = true;
     const uint32_t idesc = idesc_e4m3_f32(kGBN);
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-      for (int kb = 0; kb < KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&slot_empty[slot], slot_phase ^ 1, status, kGWaitLimit, kWaitMmaTmemEmpty, kb))) {
+      const Item it = get_item(w);
+      for (int kb = 0; kb < it.KB; ++kb) {
+        if (!__all_sync(0xffffffffu, BFP8_TIMED_WAIT(2, mbar_wait(&slot_empty[slot], slot_phase ^ 1, status, kGWaitLimit, kWaitMmaTmemEmpty, kb)))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int hf = 0; hf < C::kHalves && ok; ++hf) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, status, kGWaitLimit, kWaitMmaFull, kb))) {
+        for (int hf = 0; hf < it.halves && ok; ++hf) {
+          if (!__all_sync(0xffffffffu, BFP8_TIMED_WAIT(1, mbar_wait(&full[stage], phase, status, kGWaitLimit, kWaitMmaFull, kb)))) {
             ok = false;
             break;
           }
@@ -432,20 +656,29 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
     int slot = 0;
     uint32_t slot_phase = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-      const BTile ti = decode_item(w, args.MT, args.E, tile_off, cnt_sm, off_sm);
+      const Item it = get_item(w);
+      const BTile &ti = it.ti;
+      const int KB = it.KB;
       named_bar_sync(1, 128);                   // the previous item's scales and row info are read
+      bool ok = true;
+      if (it.second && lane == 0) ok = wait_counter(args.sync + 1 + ti.g, args.MT, status, kGWaitLimit, w);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       // this item's scales: the weight blocks of its tile(s) and the token rows
-      for (int i = et; i < C::kHalves * KB; i += 128) {
+      // (h scales of the single launch: written by other CTAs, read from L2)
+      const float *wsc = it.second ? args.w_scales2 : args.w_scales;
+      const float *xsc = it.second ? args.x_scales2 : args.x_scales;
+      for (int i = et; i < it.halves * KB; i += 128) {
         const int hf = i / KB, kb = i - hf * KB;
-        const int wrow = PHASE == 1 ? ti.e * (2 * args.I / 128) + hf * (args.I / 128) + ti.mt
-                                    : ti.e * (args.H / 128) + ti.mt;
-        sw[i] = __ldg(args.w_scales + (size_t)wrow * KB + kb);
+        const int wrow = it.l1 ? ti.e * (2 * args.I / 128) + hf * (args.I / 128) + ti.mt
+                               : ti.e * (args.H / 128) + ti.mt;
+        sw[i] = __ldg(wsc + (size_t)wrow * KB + kb);
       }
       for (int i = et; i < KB * kGBN; i += 128) {
         const int kb = i / kGBN, c = i - kb * kGBN;
-        sx[i] = c < ti.valid ? __ldg(args.x_scales + (size_t)(ti.s0 + c) * KB + kb) : 0.f;
+        const float *src = xsc + (size_t)(ti.s0 + c) * KB + kb;
+        sx[i] = c < ti.valid ? (it.second ? __ldcg(src) : __ldg(src)) : 0.f;
       }
-      if (PHASE == 2 && et < ti.valid) {
+      if (!it.l1 && et < ti.valid) {
         const int p = __ldg(args.perm + ti.s0 + et);
         row_pair[et] = p;
         row_w[et] = __ldg(args.topk_w + p);
@@ -457,9 +690,8 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
         accg[c] = 0.f;
         accu[c] = 0.f;
       }
-      bool ok = true;
-      for (int kb = 0; kb < KB; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&slot_full[slot], slot_phase, status, kGWaitLimit, kWaitEpiTmemFull, kb))) {
+      for (int kb = 0; kb < KB && ok; ++kb) {
+        if (!__all_sync(0xffffffffu, BFP8_TIMED_WAIT(3, mbar_wait(&slot_full[slot], slot_phase, status, kGWaitLimit, kWaitEpiTmemFull, kb)))) {
           ok = false;
           break;
         }
@@ -467,7 +699,7 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(slot * C::kSlotCols);
         uint32_t vg[kGBN], vu[kGBN];
         tmem_ld_32x32b_x16(taddr, vg);
-        if constexpr (PHASE == 1) tmem_ld_32x32b_x16(taddr + kGBN, vu);
+        if (PHASE != 2 && it.l1) tmem_ld_32x32b_x16(taddr + kGBN, vu);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -477,7 +709,7 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
         const float sg = sw[kb];
 #pragma unroll
         for (int c = 0; c < kGBN; ++c) accg[c] = fmaf(sg * sx[kb * kGBN + c], __uint_as_float(vg[c]), accg[c]);
-        if constexpr (PHASE == 1) {
+        if (PHASE != 2 && it.l1) {
           const float su = sw[KB + kb];
 #pragma unroll
           for (int c = 0; c < kGBN; ++c) accu[c] = fmaf(su * sx[kb * kGBN + c], __uint_as_float(vu[c]), accu[c]);
@@ -488,7 +720,7 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
       if (lane == 0) vote[warp - 2] = ok ? 1 : 0;
       named_bar_sync(1, 128);
       if (!(vote[0] && vote[1] && vote[2] && vote[3])) break;
-      if constexpr (PHASE == 1) {
+      if (PHASE != 2 && it.l1) {
         // h = silu(gate) * up for feature mt*128 + r of every token column,
         // then the token's 128 features -> one E4M3 group (amax over the
         // 128 TMEM lanes: warp shuffles, then the four quadrants)
@@ -515,6 +747,16 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
             if (et == c) args.hs[(size_t)(ti.s0 + c) * (I / 128) + ti.mt] = sc;
           }
         }
+        if (kFused) {
+          // release this item's h rows to the GEMM2 items of its token tile
+          // (their h tiles are read by TMA: async proxy)
+          fence_proxy_async_global();
+          named_bar_sync(1, 128);
+          if (et == 0) {
+            __threadfence();
+            atomicAdd(args.sync + 1 + ti.g, 1);
+          }
+        }
       } else {
         // FP32 row of each pair, times its top-k weight, into y_pairs[slot][token]
 #pragma unroll
@@ -525,9 +767,40 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
             args.y_pairs[((size_t)j * args.T + t) * args.H + ti.mt * 128 + r] = accg[c] * row_w[c];
           }
         }
+        if (kFused) {
+          named_bar_sync(1, 128);
+          if (et == 0) {
+            __threadfence();
+            atomicAdd(args.sync, 1);
+          }
+        }
       }
     }
   }
+  if (kFused) {
+    // the combine, once every CTA's GEMM2 items are done (bounded wait; a
+    // failed wait leaves y unwritten and the status word set)
+    __syncthreads();
+    if (threadIdx.x == 0) *flag = wait_counter(args.sync, n2, status, kGWaitLimit, -1) ? 1 : 0;
+    __syncthreads();
+    if (*flag)
+      combine_items((int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x,
+                    reinterpret_cast<const float4 *>(args.y_pairs), args.topk_idx, args.T, args.k, args.H, args.y,
+                    true);
+  }
+#ifdef MOE_MXQ_WAIT_STATS
+  if (lane == 0) {
+    unsigned long long *acc64 = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(status) + 64);
+    for (int i = 0; i < 4; ++i)
+      if (wait_acc[i]) atomicAdd(acc64 + i, (unsigned long long)wait_acc[i]);
+    if (warp <= 2) atomicAdd(acc64 + 4 + warp, (unsigned long long)(clock64() - k_t0));
+    if (warp == 0) {
+      int n_items = 0;
+      for (int w = blockIdx.x; w < total; w += gridDim.x) ++n_items;
+      atomicAdd(acc64 + 7, (unsigned long long)n_items);
+    }
+  }
+#endif
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -542,31 +815,47 @@ int cast_grid(int64_t threads) {
   return (int)(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
 }
 
-template <int PHASE>
-int launch_bfp8_gemm(const CUtensorMap &tw, const CUtensorMap &tb, const BGemmArgs &ga, cudaStream_t st) {
-  const size_t smem = gemm_smem_bytes(ga.KB, ga.E);
+// CTAs per SM of a GEMM launch with `smem` bytes of dynamic shared memory (two
+// where shared memory allows, 1 KB reserved per CTA), 0 if it does not fit.
+int gemm_ctas_per_sm(size_t smem) {
   int dev = 0, optin = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (smem > (size_t)optin) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return 0;
+  if (smem > (size_t)optin) return 0;
+  return (size_t)kGCtasPerSm * (smem + 1024) <= (size_t)per_sm ? kGCtasPerSm : 1;
+}
+
+template <int PHASE>
+int launch_bfp8_gemm(const CUtensorMap &tw, const CUtensorMap &tb, const CUtensorMap &tw2, const CUtensorMap &tb2,
+                     const BGemmArgs &ga, cudaStream_t st) {
+  const size_t smem = gemm_smem_bytes(PHASE == 3 ? std::max(ga.KB, ga.KB2) : ga.KB, ga.E);
+  const int per = gemm_ctas_per_sm(smem);
+  if (per == 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  // the largest shared-memory carve-out, so that the CTAs per SM counted above are resident
   if (cudaFuncSetAttribute(bfp8_gemm_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(bfp8_gemm_kernel<PHASE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
-  // two CTAs per SM where shared memory allows (1 KB reserved per CTA)
-  const int per = (size_t)kGCtasPerSm * (smem + 1024) <= (size_t)per_sm ? kGCtasPerSm : 1;
-  return launch_pdl(bfp8_gemm_kernel<PHASE>, dim3(num_sms() * per), dim3(kGThreads), smem, st, tw, tb, ga);
+  return launch_pdl(bfp8_gemm_kernel<PHASE>, dim3(num_sms() * per), dim3(kGThreads), smem, st, tw, tb, tw2, tb2, ga);
 }
 
 struct BWs {
+  size_t sync_end;   // status words, then the single launch's arrival counters (zeroed per call)
   size_t idx, w, counts, offsets, perm, inv_perm, perm_scratch, xq, xs, hq, hs, y_pairs, total;
 };
+
+// arrival counters of the single launch: GEMM2 items done, then one per token tile
+int64_t bfp8_sync_ints(int64_t T, int64_t E, int64_t k) { return 1 + max_token_tiles(T * k, E, kGBN); }
 
 BWs bfp8_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   const int64_t P = T * k;
   BWs l;
   size_t off = kStatusBytes;
+  off += round_up((size_t)bfp8_sync_ints(T, E, k) * 4, 256);
+  l.sync_end = off;
   l.idx = off;          off += round_up((size_t)P * 4, 256);
   l.w = off;            off += round_up((size_t)P * 4, 256);
   l.counts = off;       off += round_up((size_t)E * 4, 256);
@@ -587,8 +876,8 @@ bool bfp8_shape_ok(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   if (H % 128 != 0 || I % 128 != 0) return false;
   if (E > 1024 || k > 32 || k > E) return false;
   if (T * k >= (int64_t(1) << 31)) return false;
-  // tensor-map row counts and the GEMMs' int arithmetic
-  if (E * 2 * I >= (int64_t(1) << 31) || E * H >= (int64_t(1) << 31)) return false;
+  // tensor-map row counts and the GEMMs' int arithmetic (tiled rows: rows * K / 128)
+  if (E * 2 * I * (H / 128) >= (int64_t(1) << 31) || E * H * (I / 128) >= (int64_t(1) << 31)) return false;
   return true;
 }
 
@@ -609,9 +898,10 @@ extern "C" int bfp8_quantize_act(const uint16_t *x, int64_t rows, int64_t K, uin
                     reinterpret_cast<uint2 *>(q), s);
 }
 
-extern "C" int bfp8_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int64_t K, uint8_t *q, float *s,
-                                    cudaStream_t stream) {
+extern "C" int bfp8_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int64_t K, int layout, uint8_t *q,
+                                    float *s, cudaStream_t stream) {
   if (G < 0 || N <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (layout != BFP8_LAYOUT_CANONICAL && layout != BFP8_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
   if (N % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (G == 0) return MOE_OK;
   if (!w || !q || !s) return MOE_ERR_INVALID_ARG;
@@ -619,7 +909,8 @@ extern "C" int bfp8_quantize_weight(const uint16_t *w, int64_t G, int64_t N, int
   const int64_t blocks = G * (N / 128) * (K / 128);
   const int64_t cap = (int64_t)num_sms() * 8;
   return launch_pdl(bfp8_weight_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)), dim3(kWqThreads), 0, stream,
-                    reinterpret_cast<const uint4 *>(w), G, N, K, reinterpret_cast<uint4 *>(q), s);
+                    reinterpret_cast<const uint4 *>(w), G, N, K, layout == BFP8_LAYOUT_TILED ? 1 : 0,
+                    reinterpret_cast<uint4 *>(q), s);
 }
 
 extern "C" size_t moe_bfp8_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k) {
@@ -631,6 +922,8 @@ extern "C" int moe_forward_bfp8(const moe_bfp8_args *a, cudaStream_t st) {
   if (!a || a->struct_size != sizeof(moe_bfp8_args)) return MOE_ERR_INVALID_ARG;
   if (a->T < 0 || a->H <= 0 || a->I <= 0 || a->E <= 0 || a->k <= 0) return MOE_ERR_INVALID_ARG;
   if (!route_mode_valid(a->route_mode)) return MOE_ERR_INVALID_ARG;
+  if (a->phases & ~(MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2)) return MOE_ERR_INVALID_ARG;
+  if (a->weight_layout != BFP8_LAYOUT_CANONICAL && a->weight_layout != BFP8_LAYOUT_TILED) return MOE_ERR_INVALID_ARG;
   if (!bfp8_shape_ok(a->T, a->H, a->I, a->E, a->k)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!a->workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(a->workspace, 256)) return MOE_ERR_MISALIGNED;
@@ -649,7 +942,7 @@ extern "C" int moe_forward_bfp8(const moe_bfp8_args *a, cudaStream_t st) {
   }
   char *ws = reinterpret_cast<char *>(a->workspace);
   int *status = reinterpret_cast<int *>(ws);
-  if (cudaMemsetAsync(ws, 0, kStatusBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (a->T == 0) {
     if (a->counts_out && cudaMemsetAsync(a->counts_out, 0, (size_t)a->E * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (a->offsets_out && cudaMemsetAsync(a->offsets_out, 0, (size_t)(a->E + 1) * 4, st) != cudaSuccess)
@@ -670,37 +963,64 @@ extern "C" int moe_forward_bfp8(const moe_bfp8_args *a, cudaStream_t st) {
   float *hs = a->hs_out ? a->hs_out : reinterpret_cast<float *>(ws + lay.hs);
   float *y_pairs = reinterpret_cast<float *>(ws + lay.y_pairs);
 
+  // weights: [rows][K] row-major, or tiled as [rows * K / 128][128]
+  const bool tiled = a->weight_layout == BFP8_LAYOUT_TILED;
+  const uint64_t w1_cols = tiled ? 128 : (uint64_t)H, w1_rows = (uint64_t)E * 2 * I * (tiled ? H / 128 : 1);
+  const uint64_t w2_cols = tiled ? 128 : (uint64_t)I, w2_rows = (uint64_t)E * H * (tiled ? I / 128 : 1);
   CUtensorMap tw1, tx, tw2, th;
-  if (!encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(a->w1q), (uint64_t)H,
-                      (uint64_t)E * 2 * I, (uint64_t)H, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!encode_tmap_2d(&tw1, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(a->w1q), w1_cols, w1_rows, w1_cols,
+                      128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)H, (uint64_t)P, (uint64_t)H, 128, kGBN,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(a->w2q), (uint64_t)I,
-                      (uint64_t)E * H, (uint64_t)I, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t *>(a->w2q), w2_cols, w2_rows, w2_cols,
+                      128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, hq, (uint64_t)I, (uint64_t)P, (uint64_t)I, 128, kGBN,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return MOE_ERR_CUDA;
 
-  int rc = launch_route(a->logits, T, E, k, a->route_mode, idx, wts, st);
-  if (rc != MOE_OK) return rc;
-  rc = launch_permute(idx, T, E, k, counts, offsets, perm, inv_perm, status, ws + lay.perm_scratch, st);
-  if (rc != MOE_OK) return rc;
-  rc = launch_pdl(bfp8_cast_kernel, dim3(cast_grid(P * (H / 128) * 16)), dim3(kCastThreads), 0, st,
-                  reinterpret_cast<const uint4 *>(a->x), P, H, static_cast<const int32_t *>(perm), k, T,
-                  reinterpret_cast<uint2 *>(xq), xs);
-  if (rc != MOE_OK) return rc;
+  const bool whole = a->phases == 0;
+  const bool small = bfp8_front_eligible(T, H, E, k);
+  int rc = MOE_OK;
+  if (whole && small) {
+    rc = launch_pdl(bfp8_front_kernel, dim3((unsigned)(H / 128)), dim3(kBFrontThreads), bfp8_front_smem((int)T, E, k),
+                    st, a->logits, reinterpret_cast<const uint4 *>(a->x), (int)T, E, k, (int)H, a->route_mode, idx, wts,
+                    counts, offsets, perm, reinterpret_cast<uint2 *>(xq), xs);
+    if (rc != MOE_OK) return rc;
+  } else if (whole) {
+    rc = launch_route(a->logits, T, E, k, a->route_mode, idx, wts, st);
+    if (rc != MOE_OK) return rc;
+    rc = launch_permute(idx, T, E, k, counts, offsets, perm, inv_perm, status, ws + lay.perm_scratch, st);
+    if (rc != MOE_OK) return rc;
+    rc = launch_pdl(bfp8_cast_kernel, dim3(cast_grid(P * (H / 128) * 16)), dim3(kCastThreads), 0, st,
+                    reinterpret_cast<const uint4 *>(a->x), P, H, static_cast<const int32_t *>(perm), k, T,
+                    reinterpret_cast<uint2 *>(xq), xs);
+    if (rc != MOE_OK) return rc;
+  }
 
   BGemmArgs g{};
   g.E = E; g.k = k; g.T = (int)T; g.H = (int)H; g.I = (int)I; g.P = (int)P;
   g.counts = counts; g.offsets = offsets; g.perm = perm; g.topk_w = wts; g.status = status;
+  g.tiled = tiled ? 1 : 0;
   g.KB = (int)(H / 128); g.MT = (int)(I / 128);
-  g.w_scales = a->w1s; g.x_scales = xs; g.hq = hq; g.hs = hs;
-  rc = launch_bfp8_gemm<1>(tw1, tx, g, st);
-  if (rc != MOE_OK) return rc;
+  g.w_scales = a->w1s; g.x_scales = xs; g.hq = hq; g.hs = hs; g.y_pairs = y_pairs;
+  if (whole && small) {
+    // GEMM1, GEMM2 and the combine in one launch (every CTA resident)
+    g.KB2 = (int)(I / 128); g.MT2 = (int)(H / 128);
+    g.w_scales2 = a->w2s; g.x_scales2 = hs;
+    g.sync = status + kStatusBytes / 4; g.topk_idx = idx; g.y = reinterpret_cast<uint4 *>(a->y);
+    return launch_bfp8_gemm<3>(tw1, tx, tw2, th, g, st);
+  }
+  if (whole || (a->phases & MOE_PHASE_GEMM1)) {
+    rc = launch_bfp8_gemm<1>(tw1, tx, tw1, tx, g, st);
+    if (rc != MOE_OK) return rc;
+  }
   g.KB = (int)(I / 128); g.MT = (int)(H / 128);
-  g.w_scales = a->w2s; g.x_scales = hs; g.y_pairs = y_pairs;
-  rc = launch_bfp8_gemm<2>(tw2, th, g, st);
-  if (rc != MOE_OK) return rc;
+  g.w_scales = a->w2s; g.x_scales = hs;
+  if (whole || (a->phases & MOE_PHASE_GEMM2)) {
+    rc = launch_bfp8_gemm<2>(tw2, th, tw2, th, g, st);
+    if (rc != MOE_OK) return rc;
+  }
+  if (!whole) return MOE_OK;
   return launch_pdl(bfp8_combine_kernel, dim3(cast_grid(T * (H / 8))), dim3(kCastThreads), 0, st,
                     reinterpret_cast<const float4 *>(y_pairs), static_cast<const int32_t *>(idx), T, k, H,
                     reinterpret_cast<uint4 *>(a->y));

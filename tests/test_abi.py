@@ -109,14 +109,14 @@ def test_bfp8_struct_layout_matches_c(tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "moe_bfp8.h"\n'
         'int main(void){printf("%zu %zu %zu %zu %zu\\n", sizeof(moe_bfp8_args), offsetof(moe_bfp8_args, route_mode),'
-        ' offsetof(moe_bfp8_args, x), offsetof(moe_bfp8_args, hs_out), offsetof(moe_bfp8_args, workspace_bytes));'
+        ' offsetof(moe_bfp8_args, x), offsetof(moe_bfp8_args, hs_out), offsetof(moe_bfp8_args, phases));'
         ' return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.run([cc, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
     got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     B = Hp.lib()
     A = B.MoeBfp8Args
-    assert got == [ctypes.sizeof(A), A.route_mode.offset, A.x.offset, A.hs_out.offset, A.workspace_bytes.offset]
+    assert got == [ctypes.sizeof(A), A.route_mode.offset, A.x.offset, A.hs_out.offset, A.phases.offset]
 
 
 def test_bfp8_host_validation_rejects_bad_arguments():
@@ -130,9 +130,10 @@ def test_bfp8_host_validation_rejects_bad_arguments():
     assert L.bfp8_quantize_act(p, 4, 128, p, ctypes.c_void_p(0x1002), s0) == B.MOE_ERR_MISALIGNED
     assert L.bfp8_quantize_act(p, 4, 128, ctypes.c_void_p(0x1004), p, s0) == B.MOE_ERR_MISALIGNED
     assert L.bfp8_quantize_act(p, 0, 128, p, p, s0) == B.MOE_OK
-    assert L.bfp8_quantize_weight(p, 1, 64, 128, p, p, s0) == B.MOE_ERR_UNSUPPORTED_SHAPE
-    assert L.bfp8_quantize_weight(p, -1, 128, 128, p, p, s0) == B.MOE_ERR_INVALID_ARG
-    assert L.bfp8_quantize_weight(p, 0, 128, 128, p, p, s0) == B.MOE_OK
+    assert L.bfp8_quantize_weight(p, 1, 64, 128, 0, p, p, s0) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.bfp8_quantize_weight(p, -1, 128, 128, 0, p, p, s0) == B.MOE_ERR_INVALID_ARG
+    assert L.bfp8_quantize_weight(p, 1, 128, 128, 2, p, p, s0) == B.MOE_ERR_INVALID_ARG
+    assert L.bfp8_quantize_weight(p, 0, 128, 128, 1, p, p, s0) == B.MOE_OK
     assert L.moe_bfp8_workspace_size(-1, 128, 128, 4, 2) == 0
     assert L.moe_bfp8_workspace_size(8, 2048, 512, 256, 8) > 8 * 8 * 2048 * 4
     a = B.MoeBfp8Args()
@@ -145,7 +146,11 @@ def test_bfp8_host_validation_rejects_bad_arguments():
     assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_UNSUPPORTED_SHAPE      # k > E
     a.k, a.route_mode = 2, 3
     assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG            # bad routing mode
-    a.route_mode = 0
+    a.route_mode, a.phases = 0, 1
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG            # bad phase mask
+    a.phases, a.weight_layout = 0, 5
+    assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG            # bad weight layout
+    a.weight_layout = 1
     assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_INVALID_ARG            # no workspace
     a.workspace = ctypes.c_void_p(0x1080)
     assert L.moe_forward_bfp8(ctypes.byref(a), s0) == B.MOE_ERR_MISALIGNED

@@ -60,20 +60,32 @@ def test_quantize_weight_bit_exact(B):
     wb = w.to(torch.bfloat16)
     q = torch.empty(3, 256, 384, dtype=torch.uint8, device="cuda")
     s = torch.empty(3, 2, 3, dtype=torch.float32, device="cuda")
-    B.bfp8_quantize_weight(wb.cuda(), q, s)
-    torch.cuda.synchronize()
     q_r, s_r = OB.quantize_weight(Hp.bits16(wb))
-    assert np.array_equal(q.cpu().numpy(), q_r)
-    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_r.view(np.uint32))
+    for layout in (B.BFP8_LAYOUT_CANONICAL, B.BFP8_LAYOUT_TILED):
+        q.zero_(); s.zero_()
+        B.bfp8_quantize_weight(wb.cuda(), q, s, layout=layout)
+        torch.cuda.synchronize()
+        got = q.cpu().numpy()
+        if layout == B.BFP8_LAYOUT_TILED:
+            got = tiled_to_canonical(got, 3, 256, 384)
+        assert np.array_equal(got, q_r), layout
+        assert np.array_equal(s.cpu().numpy().view(np.uint32), s_r.view(np.uint32)), layout
     assert s_r[1, 1, 2] == 0.0
+
+
+def tiled_to_canonical(codes: np.ndarray, G: int, N: int, K: int) -> np.ndarray:
+    """Tile-contiguous codes [G][N/128][K/128][128][128] -> row-major [G][N][K]."""
+    t = codes.reshape(G, N // 128, K // 128, 128, 128)
+    return t.transpose(0, 1, 3, 2, 4).reshape(G, N, K)
 
 
 class BSetup:
     """A workload's tokens and block-FP8 experts on the GPU, and the oracle's
     quantised view of the experts its routing touches."""
 
-    def __init__(self, B, wl, scoring="softmax", renorm=True):
+    def __init__(self, B, wl, scoring="softmax", renorm=True, layout=None):
         self.wl, self.B = wl, B
+        self.layout = B.BFP8_LAYOUT_TILED if layout is None else layout
         E, H, I = wl.E, wl.H, wl.I
         self.x, self.logits = W.tokens(wl)
         self.idx_ref, self.w_ref = O.route_topk(self.logits.numpy(), wl.k, scoring, renorm)
@@ -89,8 +101,8 @@ class BSetup:
         self.touched = sorted(touched)
         for e in range(E):
             l1, l2 = W.expert_weights(wl, e, "cuda")
-            B.bfp8_quantize_weight(l1[None].contiguous(), self.w1q[e:e + 1], self.w1s[e:e + 1])
-            B.bfp8_quantize_weight(l2[None].contiguous(), self.w2q[e:e + 1], self.w2s[e:e + 1])
+            B.bfp8_quantize_weight(l1[None].contiguous(), self.w1q[e:e + 1], self.w1s[e:e + 1], layout=self.layout)
+            B.bfp8_quantize_weight(l2[None].contiguous(), self.w2q[e:e + 1], self.w2s[e:e + 1], layout=self.layout)
             if e in touched:
                 q1, s1 = OB.quantize_weight(Hp.bits16(l1.cpu())[None])
                 q2, s2 = OB.quantize_weight(Hp.bits16(l2.cpu())[None])
@@ -98,9 +110,14 @@ class BSetup:
         torch.cuda.synchronize()
 
     def check_weights_bit_exact(self, experts):
+        H, I = self.wl.H, self.wl.I
         for e in experts:
-            assert np.array_equal(self.w1q[e].cpu().numpy(), self.w1q_ref[e]), e
-            assert np.array_equal(self.w2q[e].cpu().numpy(), self.w2q_ref[e]), e
+            q1, q2 = self.w1q[e].cpu().numpy(), self.w2q[e].cpu().numpy()
+            if self.layout == self.B.BFP8_LAYOUT_TILED:
+                q1 = tiled_to_canonical(q1, 1, 2 * I, H)[0]
+                q2 = tiled_to_canonical(q2, 1, H, I)[0]
+            assert np.array_equal(q1, self.w1q_ref[e]), e
+            assert np.array_equal(q2, self.w2q_ref[e]), e
             assert np.array_equal(self.w1s[e].cpu().numpy().view(np.uint32), self.w1s_ref[e].view(np.uint32)), e
             assert np.array_equal(self.w2s[e].cpu().numpy().view(np.uint32), self.w2s_ref[e].view(np.uint32)), e
 
@@ -121,7 +138,7 @@ class BSetup:
         B.moe_forward_bfp8(self.x.cuda(), self.logits.cuda(), self.w1q, self.w1s, self.w2q, self.w2s, k, y, ws,
                            topk_idx_out=out["idx"], topk_w_out=out["w"], counts_out=out["counts"],
                            offsets_out=out["offsets"], perm_out=out["perm"], hq_out=out["hq"],
-                           hs_out=out["hs"], route_mode=route_mode)
+                           hs_out=out["hs"], route_mode=route_mode, weight_layout=self.layout)
         torch.cuda.synchronize()
         assert B.moe_get_device_status(ws) == 0
         res = {n: t.cpu().numpy() for n, t in out.items()}
@@ -156,10 +173,11 @@ SHAPES = {
 }
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
-def test_forward_bfp8(B, name):
+@pytest.mark.parametrize("name,layout", [(n, 1) for n in SHAPES] + [("monomoe_shape", 0), ("ragged", 0)])
+def test_forward_bfp8(B, name, layout):
+    """layout 1: tile-contiguous weight codes; 0: row-major."""
     wl = SHAPES[name]
-    st = BSetup(B, wl)
+    st = BSetup(B, wl, layout=layout)
     st.check_weights_bit_exact(st.touched[:4])
     g = st.run()
     ref = OB.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, wl.k)
@@ -224,3 +242,29 @@ def test_forward_bfp8_repeatable_and_graph_capturable(B):
     torch.cuda.synchronize()
     assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
     assert torch.equal(ys[0].view(torch.int16), ys[2].view(torch.int16))
+
+
+def test_forward_bfp8_gemm_phase_reruns(B):
+    """phases = GEMM1 (or GEMM2) re-runs one GEMM on the state a whole-layer call
+    left: h comes back bit-identical and y is not touched."""
+    wl = SHAPES["ragged"]
+    st = BSetup(B, wl)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    P = T * k
+    x, logits = st.x.cuda(), st.logits.cuda()
+    ws = torch.empty(B.moe_bfp8_workspace_size(T, H, I, E, k), dtype=torch.uint8, device="cuda")
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    hq = torch.empty(P, I, dtype=torch.uint8, device="cuda")
+    hs = torch.empty(P, I // 128, dtype=torch.float32, device="cuda")
+    kw = dict(hq_out=hq, hs_out=hs)
+    B.moe_forward_bfp8(x, logits, st.w1q, st.w1s, st.w2q, st.w2s, k, y, ws, **kw)
+    torch.cuda.synchronize()
+    hq0, hs0, y0 = hq.clone(), hs.clone(), y.clone()
+    hq.zero_(); hs.zero_(); y.fill_(1.0)
+    B.moe_forward_bfp8(x, logits, st.w1q, st.w1s, st.w2q, st.w2s, k, y, ws, phases=B.PHASE_GEMM1, **kw)
+    B.moe_forward_bfp8(x, logits, st.w1q, st.w1s, st.w2q, st.w2s, k, y, ws, phases=B.PHASE_GEMM2, **kw)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ws) == 0
+    assert torch.equal(hq, hq0) and torch.equal(hs.view(torch.int32), hs0.view(torch.int32))
+    assert bool((y == 1.0).all())
+    assert not torch.equal(y.view(torch.int16), y0.view(torch.int16))
