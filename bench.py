@@ -58,7 +58,8 @@ TRAFFIC = {
 # the same for the block-FP8 variant's GEMMs (csrc/bfp8.cu)
 BFP8_SOURCES = ("bfp8.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC_BFP8 = {
-    "src_sha256": None,
+    "src_sha256": "178f15005a48c55c5c8f7d7e9c481fe306c70031bdbd44fe850fb6a7dc97dccd",
+    "small_decode": {"gemm1": 117679872 + 162816, "gemm2": 58821376 + 4096},
 }
 UNIT = "tokens/s"
 
@@ -391,6 +392,13 @@ def run_ours(args, rank, world, local_rank):
                  "algorithmic_bytes": dom_bytes, "algorithmic_flops": dom_flops,
                  "traffic": measured_traffic(wl.name, dom, bfp8), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)"})
     layer_time_bound = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (fp8_peak_tflops * 1e12))
+    # context for the fraction: a plain PyTorch read (sum) of the same number of
+    # bytes, cold L2 like the kernel -- short reads do not reach the long-copy peak
+    read_buf = torch.ones(max(dom_bytes // 4, 1), dtype=torch.float32, device=dev)
+    read_out = torch.empty((), dtype=torch.float32, device=dev)
+    rt = timed_loop(lambda: torch.sum(read_buf, dim=(0,), out=read_out), max(args.steps, 20))
+    read_ms = statistics.median(rt)
+    del read_buf
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -406,6 +414,10 @@ def run_ours(args, rank, world, local_rank):
         "layer_roofline_frac": round(layer_time_bound / (mean_ms * 1e-3), 4),
         "gemm_ms": {"gemm1": round(g1_ms, 5), "gemm2": round(g2_ms, 5)},
         "roofline": roof,
+        "same_size_read": {"bytes": dom_bytes, "ms": round(read_ms, 5),
+                           "gbs": round(dom_bytes / (read_ms * 1e-3) / 1e9, 1),
+                           "what": "torch.sum over a float32 buffer of the dominant kernel's algorithmic bytes, "
+                                   "L2 flushed before each call (median)"},
         "gpu_launches": n_launch_forward * args.steps,
         "wall_s_timed_region": round(wall, 4),
         "clocks": clk.summary(),
