@@ -222,6 +222,25 @@ def algorithmic_bfp8(wl, counts):
     }
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of per-rank floats over the process group (the
+    slowest rank decides a timed region); the values themselves for one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def replica_tokens_per_s(world, tokens, steps, total_ms):
+    """Whole-job throughput of `world` independent replicas that each processed
+    `tokens` per step for `steps` steps within the max-over-ranks `total_ms`."""
+    return world * tokens * steps / (total_ms / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -327,13 +346,8 @@ def run_ours(args, rank, world, local_rank):
             if world > 1:
                 torch.distributed.barrier()
         assert B.moe_get_device_status(ws, stream) == 0, "device status word reports an error"
-        total_ms = sum(times)
-        mean_ms = total_ms / len(times)
-        if world > 1:
-            t = torch.tensor([total_ms, mean_ms], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            total_ms, mean_ms = float(t[0]), float(t[1])
-        value = world * T * args.steps / (total_ms / 1e3)
+        total_ms, mean_ms = max_over_ranks([sum(times), sum(times) / len(times)], world, dev)
+        value = replica_tokens_per_s(world, T, args.steps, total_ms)
 
     # per-GEMM timing (dominant kernel) with the layer's own routing
     if bfp8:
@@ -436,12 +450,8 @@ def run_ours(args, rank, world, local_rank):
             y_h.copy_(y, non_blocking=True)
 
         e2e_times = timed_loop(e2e_step, args.steps)
-        e2e_total = sum(e2e_times)
-        if world > 1:
-            t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_total = float(t[0])
-        result["e2e"] = {"value": round(world * T * args.steps / (e2e_total / 1e3), 1), "unit": UNIT,
+        e2e_total = max_over_ranks([sum(e2e_times)], world, dev)[0]
+        result["e2e"] = {"value": round(replica_tokens_per_s(world, T, args.steps, e2e_total), 1), "unit": UNIT,
                          "h2d_bytes_per_step": x_h.numel() * 2 + l_h.numel() * 4,
                          "d2h_bytes_per_step": y_h.numel() * 2}
         if rank == 0 and world == 1:
