@@ -105,7 +105,9 @@ MOE_API size_t moe_bfp8_workspace_size(int64_t T, int64_t H, int64_t I, int32_t 
 
 /* The whole block-FP8 layer: routing, permute, cast of x into pool rows,
  * GEMM1 + SiLU(gate)*up + FP8 write-back, GEMM2, weighted combine.  Device
- * waits are bounded (MOE_ERR_TIMEOUT in the workspace status word). */
+ * waits are bounded (MOE_ERR_TIMEOUT in the workspace status words, read with
+ * moe_get_device_status); the debug hook MOE_MXQ_DEBUG_INJECT_WAIT described
+ * in moe_mxq.h applies to these GEMM launches too. */
 MOE_API int moe_forward_bfp8(const moe_bfp8_args *args, cudaStream_t stream);
 
 #ifdef __cplusplus

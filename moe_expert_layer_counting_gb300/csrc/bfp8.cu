@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "../../include/moe_bfp8.h"
 #include "host_common.h"
@@ -270,10 +271,11 @@ constexpr int kGThreads = 192;
 constexpr int kGCtasPerSm = 2;
 constexpr uint32_t kGTmemCols = 128;
 constexpr long long kGWaitLimit = 2000000000LL;
+constexpr long long kGInjectedWaitLimit = 20000000LL;  // ~10 ms: the debug wait's budget
 constexpr int kGOffA = 0;
 constexpr int kGOffB = kGOffA + kGStages * kGTileA;
 constexpr int kGOffBar = kGOffB + kGStages * kGTileB;
-constexpr int kGNumBars = 2 * kGStages + 2 * 8 + 1;   // full/empty stages, full/empty slots (<= 8), MMAs done
+constexpr int kGNumBars = 2 * kGStages + 2 * 8 + 2;   // full/empty stages, full/empty slots (<= 8), MMAs done, debug
 constexpr int kGOffMisc = kGOffBar + 256;             // tmem ptr, votes, column maxima, row info
 constexpr int kGOffScan = kGOffMisc + 512;
 constexpr int kGOffSc = kGOffScan + 64;               // scales: weights [2][KB], tokens [KB][16]
@@ -304,6 +306,7 @@ struct BGemmArgs {
   int KB2, MT2;                    // PHASE 3: GEMM2's
   int P;                           // pool rows (T * k, dropped pairs excluded from the tiles)
   int tiled;                       // weight codes tile-contiguous (else row-major)
+  int inject_wait;                 // debug: 1 = the MMA warp first waits on a barrier nothing completes
   const int32_t *counts, *offsets, *perm;
   const float *topk_w;             // [T*k] by pair id
   const float *w_scales;           // GEMM1: [E][2I/128][KB]; GEMM2: [E][H/128][KB]
@@ -443,6 +446,7 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
   uint64_t *slot_full = bars + 2 * kGStages;
   uint64_t *slot_empty = slot_full + 8;
   uint64_t *mma_done = slot_empty + 8;
+  uint64_t *never = mma_done + 1;           // debug wait target: initialised, never arrived on
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + kGOffMisc);
   int *flag = reinterpret_cast<int *>(smem + kGOffMisc + 8);            // combine go-ahead
   int *vote = reinterpret_cast<int *>(smem + kGOffMisc + 16);           // [4]
@@ -484,6 +488,7 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
         mbar_init(&slot_empty[s], 4);
       }
       mbar_init(mma_done, 1);
+      mbar_init(never, 1);
       fence_mbar_init();
     }
     __syncwarp();
@@ -613,6 +618,10 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
     const uint32_t idesc = idesc_e4m3_f32(kGBN);
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
       const Item it = get_item(w);
+      // failure-detection test hook: a wait that can only end by its timeout
+      if (args.inject_wait == 1 && w == (int)blockIdx.x &&
+          !__all_sync(0xffffffffu, mbar_wait(never, 0, status, kGInjectedWaitLimit, kWaitInjected, w)))
+        break;
       for (int kb = 0; kb < it.KB; ++kb) {
         if (!__all_sync(0xffffffffu, BFP8_TIMED_WAIT(2, mbar_wait(&slot_empty[slot], slot_phase ^ 1, status, kGWaitLimit, kWaitMmaTmemEmpty, kb)))) {
           ok = false;
@@ -839,7 +848,10 @@ int launch_bfp8_gemm(const CUtensorMap &tw, const CUtensorMap &tb, const CUtenso
       cudaFuncSetAttribute(bfp8_gemm_kernel<PHASE>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
           cudaSuccess)
     return MOE_ERR_CUDA;
-  return launch_pdl(bfp8_gemm_kernel<PHASE>, dim3(num_sms() * per), dim3(kGThreads), smem, st, tw, tb, tw2, tb2, ga);
+  BGemmArgs g = ga;
+  // debug hook of the failure-detection tests (see moe_get_device_status)
+  if (const char *env = getenv("MOE_MXQ_DEBUG_INJECT_WAIT")) g.inject_wait = atoi(env);
+  return launch_pdl(bfp8_gemm_kernel<PHASE>, dim3(num_sms() * per), dim3(kGThreads), smem, st, tw, tb, tw2, tb2, g);
 }
 
 struct BWs {

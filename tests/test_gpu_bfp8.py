@@ -268,3 +268,35 @@ def test_forward_bfp8_gemm_phase_reruns(B):
     assert torch.equal(hq, hq0) and torch.equal(hs.view(torch.int32), hs0.view(torch.int32))
     assert bool((y == 1.0).all())
     assert not torch.equal(y.view(torch.int16), y0.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["monomoe_shape", "ragged"])
+def test_forward_bfp8_injected_wait_times_out_then_recovers(B, monkeypatch, name):
+    """MOE_MXQ_DEBUG_INJECT_WAIT=1: each CTA's MMA warp first waits on a barrier
+    nothing completes; the wait gives up (~10 ms), records MOE_ERR_TIMEOUT at
+    site 7, raises the abort flag, every other wait of the launch (stages,
+    TMEM slots, arrival counters of the single launch) gives up, and the next
+    call in the same process is correct.  monomoe_shape: front + single
+    launch; ragged: the chain of separate launches."""
+    import time
+    wl = SHAPES[name]
+    st = BSetup(B, wl)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    x, logits = st.x.cuda(), st.logits.cuda()
+    ws = torch.empty(B.moe_bfp8_workspace_size(T, H, I, E, k), dtype=torch.uint8, device="cuda")
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    B.moe_forward_bfp8(x, logits, st.w1q, st.w1s, st.w2q, st.w2s, k, y, ws)
+    torch.cuda.synchronize()
+    monkeypatch.setenv("MOE_MXQ_DEBUG_INJECT_WAIT", "1")
+    t0 = time.perf_counter()
+    B.moe_forward_bfp8(x, logits, st.w1q, st.w1s, st.w2q, st.w2s, k, y, ws)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    words = ws[:20].view(torch.int32).cpu().tolist()
+    assert B.moe_get_device_status(ws) == B.MOE_ERR_TIMEOUT, words
+    assert words[1] == 1 and words[2] == 7, words
+    assert elapsed < 5.0, f"the failing call took {elapsed:.2f} s"
+    monkeypatch.delenv("MOE_MXQ_DEBUG_INJECT_WAIT")
+    g = st.run()
+    ref = OB.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, k)
+    Hp.assert_bf16_close(g["y"], ref["y"], what=name)
