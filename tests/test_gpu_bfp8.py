@@ -300,3 +300,21 @@ def test_forward_bfp8_injected_wait_times_out_then_recovers(B, monkeypatch, name
     g = st.run()
     ref = OB.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, k)
     Hp.assert_bf16_close(g["y"], ref["y"], what=name)
+
+
+def test_bfp8_layer_container_fewer_tokens_than_capacity(B):
+    """layer.MoELayerBfp8 sized for 64 tokens, called with 37: the workspace is
+    sliced to the call's size and the result matches the oracle on those tokens."""
+    from moe_expert_layer_counting_gb300.layer import Bfp8Experts, MoELayerBfp8
+    wl = W.WORKLOADS["tiny"]
+    x, logits = W.tokens(wl)
+    l1, l2 = W.all_expert_weights(wl, "cpu")
+    layer = MoELayerBfp8(Bfp8Experts.from_bf16(l1.cuda(), l2.cuda()), wl.k, max_tokens=64)
+    n = 37
+    y = layer(x[:n].contiguous().cuda(), logits[:n].contiguous().cuda())
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    q1, s1 = OB.quantize_weight(Hp.bits16(l1))
+    q2, s2 = OB.quantize_weight(Hp.bits16(l2))
+    ref = OB.forward(Hp.bits16(x[:n]), logits[:n].numpy(), q1, s1, q2, s2, wl.k)
+    Hp.assert_bf16_close(Hp.bits16(y.cpu()), ref["y"], what="MoELayerBfp8")
