@@ -58,8 +58,8 @@ TRAFFIC = {
 # the same for the block-FP8 variant's GEMMs (csrc/bfp8.cu)
 BFP8_SOURCES = ("bfp8.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC_BFP8 = {
-    "src_sha256": "178f15005a48c55c5c8f7d7e9c481fe306c70031bdbd44fe850fb6a7dc97dccd",
-    "small_decode": {"gemm1": 117679872 + 162816, "gemm2": 58821376 + 4096},
+    "src_sha256": "91bd917e9e7a5b05fd040c27d223d855310a56b6268a544a86ac9ca95e851c8d",
+    "small_decode": {"gemm1": 117676544 + 58880, "gemm2": 58821632 + 256},
 }
 UNIT = "tokens/s"
 
