@@ -58,8 +58,8 @@ TRAFFIC = {
 # the same for the block-FP8 variant's GEMMs (csrc/bfp8.cu)
 BFP8_SOURCES = ("bfp8.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC_BFP8 = {
-    "src_sha256": "91bd917e9e7a5b05fd040c27d223d855310a56b6268a544a86ac9ca95e851c8d",
-    "small_decode": {"gemm1": 117676544 + 58880, "gemm2": 58821632 + 256},
+    "src_sha256": "29ff1ef0a0028b43fb3a4f0da822dcb433f7974b4f09276cbad094a1457b5186",
+    "small_decode": {"gemm1": 117679360 + 427264, "gemm2": 58838272 + 57088},
 }
 UNIT = "tokens/s"
 

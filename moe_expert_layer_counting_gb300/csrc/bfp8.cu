@@ -1,12 +1,16 @@
 // bfp8.cu -- the block-FP8 variant of the MoE expert layer on sm_103a.
 //
 // Format (MonoMoe kernel -- design, "Fixed shape"): E4M3 weights with one
-// float32 scale per 128 x 128 block, E4M3 activations with one float32 scale
-// per 128 values of a row along K.  Pipeline (same page, section 1): routing
-// and the counting-sort permute (the layer's own kernels), the BF16 -> FP8
-// cast of x into expert-major pool rows, GEMM1 (gate and up) with SiLU(gate)
-// * up and an FP8 write-back of h, GEMM2, and a combine that sums the k
-// weighted FP32 partials of each token and casts once to BF16.
+// float32 scale per 128 x 128 block (codes row-major or tile-contiguous, one
+// 16 KB piece per block), E4M3 activations with one float32 scale per 128
+// values of a row along K.  Pipeline (same page, section 1): routing and the
+// counting-sort permute, the BF16 -> FP8 cast of x into expert-major pool
+// rows, GEMM1 (gate and up) with SiLU(gate) * up and an FP8 write-back of h,
+// GEMM2, and a combine that sums the k weighted FP32 partials of each token
+// and casts once to BF16.  Small problems (T <= 64, E <= 256) run it as two
+// launches: bfp8_front_kernel (routing + permute + cast) and one resident
+// launch of GEMM1 + GEMM2 + combine; larger ones as the layer's routing and
+// permute kernels, the pool cast, GEMM1, GEMM2 and the combine.
 //
 // The scales are plain float32 values, so the block-scaled MMA (power-of-two
 // scales per 32) cannot carry them.  Each 128-wide K block is instead one
@@ -672,6 +676,7 @@ __global__ void __launch_bounds__(kGThreads, kGCtasPerSm)
       bool ok = true;
       if (it.second && lane == 0) ok = wait_counter(args.sync + 1 + ti.g, args.MT, status, kGWaitLimit, w);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      __syncwarp();                             // the other lanes' h-scale reads come after lane 0's acquire
       // this item's scales: the weight blocks of its tile(s) and the token rows
       // (h scales of the single launch: written by other CTAs, read from L2)
       const float *wsc = it.second ? args.w_scales2 : args.w_scales;

@@ -7,8 +7,9 @@ relative -- the two sides' h differ by float32 accumulation), y within the
 layer's tolerance (relative Frobenius error <= 5e-3, max error <= 1e-2 of
 max |y|).  Shapes cover the MonoMoe kernel design's fixed shape (8 tokens,
 E = 256, H = 2048, I = 512, top-8), several token tiles per expert, one
-token, k = 1, a 7168-wide hidden size, ragged counts and E not a multiple
-of 32."""
+token, k = 1, a 7168-wide hidden size, ragged counts, E not a multiple
+of 32, E = 300 (the chain of separate launches), and more GEMM1 items than
+CTAs on both launch paths."""
 import numpy as np
 import pytest
 import torch
@@ -47,6 +48,25 @@ def test_quantize_act_bit_exact(B, rows, K, seed):
     B.bfp8_quantize_act(x.cuda(), q, s)
     torch.cuda.synchronize()
     q_r, s_r = OB.quantize_act(Hp.bits16(x))
+    assert np.array_equal(q.cpu().numpy(), q_r)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_r.view(np.uint32))
+
+
+def test_quantize_act_tiny_and_huge_groups_bit_exact(B):
+    """Groups whose float32 scale is subnormal (BF16 values down to 2^-133, scale
+    = amax / 448 below 2^-126) and groups near the BF16 maximum: the divides are
+    IEEE round-to-nearest with subnormals on both sides, codes saturate at 448."""
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(6, 1024, generator=g)
+    exps = torch.tensor([-133, -131, -128, -126, -120, 120, 124, 125], dtype=torch.float32)
+    x = (x.view(6, 8, 128) * torch.exp2(exps)[None, :, None]).view(6, 1024)
+    xb = x.to(torch.bfloat16)
+    q = torch.empty(6, 1024, dtype=torch.uint8, device="cuda")
+    s = torch.empty(6, 8, dtype=torch.float32, device="cuda")
+    B.bfp8_quantize_act(xb.cuda(), q, s)
+    torch.cuda.synchronize()
+    q_r, s_r = OB.quantize_act(Hp.bits16(xb))
+    assert np.any((s_r > 0) & (s_r < np.float32(2.0 ** -126)))      # subnormal scales occur
     assert np.array_equal(q.cpu().numpy(), q_r)
     assert np.array_equal(s.cpu().numpy().view(np.uint32), s_r.view(np.uint32))
 
@@ -170,6 +190,11 @@ SHAPES = {
     "ragged": W.Workload("bfp8_ragged", T=100, H=384, I=256, E=37, k=4, sigma=0.03, seed=22),
     "wide_H": W.Workload("bfp8_wide", T=3, H=7168, I=256, E=9, k=2, sigma=0.01, seed=23),
     "k1": W.Workload("bfp8_k1", T=40, H=512, I=256, E=10, k=1, sigma=0.03, seed=24),
+    # E > 256: routing, permute and cast as separate launches, then the separate GEMMs
+    "wide_E": W.Workload("bfp8_wideE", T=5, H=256, I=128, E=300, k=4, sigma=0.05, seed=25),
+    # more GEMM1 items than CTAs (several items per CTA), single launch / chain
+    "many_items_single": W.Workload("bfp8_many1", T=64, H=256, I=2048, E=64, k=8, sigma=0.02, seed=26),
+    "many_items_chain": W.Workload("bfp8_many2", T=100, H=256, I=2048, E=64, k=8, sigma=0.02, seed=27),
 }
 
 
