@@ -192,6 +192,8 @@ SHAPES = {
     "k1": W.Workload("bfp8_k1", T=40, H=512, I=256, E=10, k=1, sigma=0.03, seed=24),
     # E > 256: routing, permute and cast as separate launches, then the separate GEMMs
     "wide_E": W.Workload("bfp8_wideE", T=5, H=256, I=128, E=300, k=4, sigma=0.05, seed=25),
+    # E = 1, k = 1: every pair on one expert, three token tiles (the last ragged)
+    "one_expert": W.Workload("bfp8_one_expert", T=40, H=256, I=128, E=1, k=1, sigma=0.05, seed=28),
     # more GEMM1 items than CTAs (several items per CTA), single launch / chain
     "many_items_single": W.Workload("bfp8_many1", T=64, H=256, I=2048, E=64, k=8, sigma=0.02, seed=26),
     "many_items_chain": W.Workload("bfp8_many2", T=100, H=256, I=2048, E=64, k=8, sigma=0.02, seed=27),
