@@ -27,6 +27,7 @@ SHAPES = {
     "pool_cast": (100, 256, 128, 24, 4),        # T > 64: routing + permute + pool cast
     "wide_H_front": (3, 7168, 128, 9, 2),       # front kernel, 224 column groups
     "large_path": (2048, 1024, 128, 64, 8),     # P*H > 16M: activation cast + pool copy, 224-token tiles
+    "one_expert": (40, 256, 128, 1, 1),         # front kernel, E = 1, k = 1: three token tiles of one expert
 }
 
 
