@@ -58,3 +58,24 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "1"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_json_line_both_weight_formats():
+    """Rank 0 of the reference arm prints one JSON line with the contract's keys
+    (the oracle timed on the host cores), for both weight formats."""
+    import json
+    for extra in ([], ["--weights", "bfp8"]):
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                            "tiny", "--steps", "1", "--warmup", "1", *extra],
+                           env=dict(os.environ, RANK="0", WORLD_SIZE="1"), capture_output=True, text=True,
+                           timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        lines = [l for l in r.stdout.splitlines() if l.strip()]
+        assert len(lines) == 1
+        d = json.loads(lines[0])
+        assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
+        assert d["higher_is_better"] is True and d["dtype"] == "f64"
+        assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}
+        assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+        assert ("block-FP8" in d["config"]["workload"]) == bool(extra)
