@@ -222,6 +222,13 @@ def algorithmic_bfp8(wl, counts):
     }
 
 
+def layer_rates(alg, ms_per_step):
+    """Whole-layer rates of one step: algorithmic GB/s and TFLOP/s."""
+    sec = ms_per_step * 1e-3
+    return {"gbs": round(alg["layer_bytes"] / sec / 1e9, 1), "tflops": round(alg["layer_flops"] / sec / 1e12, 3),
+            "algorithmic_bytes": alg["layer_bytes"], "algorithmic_flops": alg["layer_flops"]}
+
+
 # ---------------------------------------------------------------- ranks
 
 def max_over_ranks(values, world, device="cpu"):
@@ -431,6 +438,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "flushed between steps (512 MiB write + 512 MiB read)" if not args.no_flush else "not flushed",
                    "cuda_graph": True, "parallelism": "replicas" if world > 1 else "single GPU"},
         "layer_roofline_frac": round(layer_time_bound / (mean_ms * 1e-3), 4),
+        "layer_rates": layer_rates(alg, mean_ms),
         "gemm_ms": {"gemm1": round(g1_ms, 5), "gemm2": round(g2_ms, 5)},
         "roofline": roof,
         "same_size_reference": {"bytes": dom_bytes,

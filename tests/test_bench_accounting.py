@@ -49,3 +49,10 @@ def test_launches_per_forward():
     assert bench.launches_per_forward_bfp8(128, 7168, 256, 8) == 6
     # prefill: quant, route, permute (count + scatter), pool prep, GEMM1, GEMM2, combine
     assert bench.launches_per_forward(4096, 7168, 256, 8) == 8
+
+
+def test_layer_rates():
+    alg = {"layer_bytes": 94_000_000, "layer_flops": 402_653_184}
+    r = bench.layer_rates(alg, 0.0394)                 # 39.4 us per step
+    assert r["gbs"] == round(94e6 / 39.4e-6 / 1e9, 1)
+    assert r["tflops"] == round(402653184 / 39.4e-6 / 1e12, 3)
