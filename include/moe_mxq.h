@@ -158,8 +158,10 @@ MOE_API int moe_permute(const int32_t *topk_idx, int64_t T, int32_t E, int32_t k
  * array (moe_permute_workspace_size(T,E,k) - 256 > the maximum, e.g. E = 1024
  * with more than 32768 pairs); MOE_ERR_CUDA if the array's device address
  * cannot be looked up.
- * The first call on each device looks up the array's address (once, with
- * that device current); make that first call before any stream capture.
+ * The first call on each device looks up the array's address (once per
+ * device and context, with that device current; a device reset replaces the
+ * context and the next call looks it up again); make that first call before
+ * any stream capture.
  * All calls on a device share the array, which keeps the last call's
  * contents: calls that overlap on the GPU race. */
 #define MOE_PERMUTE_NOALLOC_MAX_HIST_BYTES 65536

@@ -33,20 +33,57 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_permute_scratch[kStatusBytes + kHistBytes];
 
 std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+struct CachedAddress {
+  unsigned long long ctx_id;   // context the address belongs to (0: none yet)
+  void *ptr;
+};
+CachedAddress g_scratch[kMaxDevices] = {};
 
-// Looks up the device address of the scratch array once per device, with
-// that device current.  Returns nullptr if the lookup fails.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Id of the current context, or 0 if the driver does not report one.  A
+// device reset (cudaDeviceReset, or a framework that resets the device)
+// replaces the context, and with it the array's device address.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Looks up the device address of the scratch array with the device current:
+// once per device and context (again after a reset replaced the context;
+// on every call while the driver reports no context id, e.g. before the
+// runtime created the device's context, which the lookup itself does).  Returns nullptr if the
+// lookup fails.
 void *scratch_for_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
+  CachedAddress &c = g_scratch[dev];
+  if (ctx == 0 || c.ctx_id != ctx || !c.ptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return nullptr;
-    g_scratch_ptr[dev] = p;
+    c.ctx_id = ctx;
+    c.ptr = p;
   }
-  return g_scratch_ptr[dev];
+  return c.ptr;
 }
 
 }  // namespace

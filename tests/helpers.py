@@ -135,3 +135,71 @@ def check_requantised_h(hq_g, hs_g, hq_r, hs_r, amax_ref=None, max_code_frac=1e-
     assert frac <= max_code_frac, f"{frac:.2e} of FP8 codes differ (> {max_code_frac})"
     assert smis.sum() <= max(1, int(1e-3 * smis.size)), f"{int(smis.sum())} scale bytes differ"
     return frac, int(smis.sum())
+
+
+# ---------------------------------------------------------------- the oracle on many large experts
+
+def oracle_pool(workers=None):
+    """Process pool for running the oracle on many large experts at once.
+
+    Started with the spawn method, so it is safe to create after CUDA was
+    initialised in this process (a forked child of a CUDA process can hang)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    n = workers or max(1, min(16, len(os.sched_getaffinity(0))))
+    return cf.ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn"))
+
+
+def sample_tokens(idx: np.ndarray, counts: np.ndarray, n_random: int, seed: int) -> np.ndarray:
+    """Tokens of a large workload whose output rows are compared with the oracle.
+
+    For each of the two hottest and the two coldest non-empty experts: its
+    first and last token (an expert's last token sits in its ragged last token
+    tile), all of its tokens when it has at most three; the last two tokens
+    of expert 0 (the hottest expert of the skewed workload); then
+    ``n_random`` further tokens drawn with ``seed``."""
+    T = idx.shape[0]
+    nz = np.nonzero(counts)[0]
+    order = nz[np.argsort(counts[nz], kind="stable")]
+    pick = set()
+    for e in list(order[:2]) + list(order[-2:]):
+        toks = np.nonzero((idx == e).any(axis=1))[0]
+        pick.update(int(t) for t in (toks if toks.size <= 3 else (toks[0], toks[-1])))
+    t0 = np.nonzero((idx == 0).any(axis=1))[0]
+    pick.update(int(t) for t in t0[-2:])
+    rng = np.random.default_rng(seed)
+    rest = np.setdiff1d(np.arange(T), np.array(sorted(pick), dtype=np.int64))
+    pick.update(int(t) for t in rng.choice(rest, size=min(n_random, rest.size), replace=False))
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def oracle_forward_tokens(pool, x_bits, logits, weights, k, chunk=2):
+    """The oracle's layer on a few tokens, its per-expert work spread over ``pool``.
+
+    Same steps as ``oracle.moe.forward``: the oracle's activation cast and
+    routing of these tokens, then ``oracle.moe.expert_forward`` per group of
+    ``chunk`` experts (the expert ids renumbered inside each group, the
+    other experts' pairs marked dropped), each pair's row taken from the group
+    that holds its expert, and ``oracle.moe.combine``.  ``weights`` maps an
+    expert id to its oracle-quantised (w1q, w1s, w2q, w2s); it must hold
+    every expert the tokens route to."""
+    from oracle import moe as O
+    xq, xs = O.quantize_act(x_bits)
+    idx, w = O.route_topk(logits, k)
+    experts = sorted(set(int(e) for e in idx.reshape(-1)))
+    missing = [e for e in experts if e not in weights]
+    assert not missing, f"oracle weights missing for experts {missing}"
+    jobs = []
+    for c in range(0, len(experts), chunk):
+        sub = experts[c:c + chunk]
+        local = np.full(idx.shape, -1, np.int32)
+        for i, e in enumerate(sub):
+            local[idx == e] = i
+        ws = [np.stack([weights[e][j] for e in sub]) for j in range(4)]
+        jobs.append((local, pool.submit(O.expert_forward, xq, xs, *ws, local, w, len(sub))))
+    y_pairs = np.zeros((k, idx.shape[0], xq.shape[1]), np.uint16)
+    for local, fut in jobs:
+        yp = fut.result()
+        mine = (local >= 0).T                                  # [k, T]
+        y_pairs[mine] = yp[mine]
+    return {"topk_idx": idx, "topk_w": w, "y_pairs": y_pairs, "y": O.combine(y_pairs, idx)}

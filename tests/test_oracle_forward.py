@@ -166,3 +166,22 @@ def test_tiny_against_scalar_loop_implementation():
     ref = _scalar_loop_layer(xb, logits.numpy(), w1q, w1s, w2q, w2s, wl.k, toks)
     for t in toks:
         assert np.array_equal(out["y"][t], ref[t]), t
+
+
+def test_pooled_sampled_tokens_equal_the_oracle_forward():
+    """The large-workload parity test runs the oracle on a sample of tokens
+    with its per-expert work spread over a process pool; that orchestration
+    gives exactly oracle.moe.forward's rows for those tokens (Tiny, every
+    token of a sample that includes both ends of each expert)."""
+    from tests import helpers as Hp
+    T, H, I, E, k = 40, 64, 64, 6, 2
+    x, logits, w1q, w1s, w2q, w2s = _small_layer(T, H, I, E, k, seed=11)
+    full = O.forward(x, logits, w1q, w1s, w2q, w2s, k)
+    toks = Hp.sample_tokens(full["topk_idx"], full["counts"], n_random=3, seed=5)
+    assert 0 < toks.size < T
+    weights = {e: (w1q[e], w1s[e], w2q[e], w2s[e]) for e in range(E)}
+    with Hp.oracle_pool(workers=2) as pool:
+        got = Hp.oracle_forward_tokens(pool, x[toks], logits[toks], weights, k, chunk=2)
+    assert np.array_equal(got["topk_idx"], full["topk_idx"][toks])
+    assert np.array_equal(got["y_pairs"], full["y_pairs"][:, toks])
+    assert np.array_equal(got["y"], full["y"][toks])

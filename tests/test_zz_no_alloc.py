@@ -1,8 +1,10 @@
 """moe_permute_noalloc: the permute for callers that cannot allocate device
 memory (its scratch is the library's own device array).  Checked through the
-C ABI against moe_permute (the entry point with a caller workspace) on the
-same inputs, on two calls in a row, so that contents left in the shared
-array by one call cannot change the next call's result.
+C ABI against the oracle's permute and against moe_permute (the entry point
+with a caller workspace) on the same inputs, on two calls in a row, so that
+contents left in the shared array by one call cannot change the next call's
+result; with the device status written to a caller buffer and to the
+library's own array.
 
 This file is collected last on purpose (pytest collects test files in name
 order): a failure here comes after every other test has run."""
@@ -48,23 +50,37 @@ def _outputs(E, P):
             torch.full((P,), -3, dtype=torch.int32, device=dev))
 
 
+@pytest.mark.parametrize("status_out", ["caller", "library"])
 @pytest.mark.parametrize("case", _cases(), ids=lambda c: c[0])
-def test_noalloc_permute_matches_workspace_permute(B, case):
+def test_noalloc_permute_matches_oracle_and_workspace_permute(B, case, status_out):
+    """Two calls in a row, each bit-exact against the oracle's permute and
+    equal to moe_permute's outputs.  status_out = "caller": the device status
+    goes to a caller buffer; "library": to the library's own array (no
+    device_status argument), read back through the outputs only."""
     _, idx_np, E = case
     T, k = idx_np.shape
     P = T * k
+    c_ref, o_ref, p_ref, i_ref = O.permute(idx_np, E)
+    n = int(o_ref[-1])
     idx = torch.from_numpy(idx_np).cuda()
     ws = torch.empty(B.moe_permute_workspace_size(T, E, k), dtype=torch.uint8, device="cuda")
     ref = _outputs(E, P)
     B.moe_permute(idx, E, *ref, ws)
     for call in range(2):
         got = _outputs(E, P)
-        st = torch.full((1,), 99, dtype=torch.int32, device="cuda")
+        st = torch.full((1,), 99, dtype=torch.int32, device="cuda") if status_out == "caller" else None
         B.moe_permute_noalloc(idx, E, *got, device_status=st)
         torch.cuda.synchronize()
+        counts, offsets, perm, inv = (t.cpu().numpy() for t in got)
+        assert np.array_equal(counts, c_ref), f"call {call}"
+        assert np.array_equal(offsets, o_ref), f"call {call}"
+        assert np.array_equal(perm[:n], p_ref), f"call {call}"
+        assert np.all(perm[n:] == -3), f"call {call}: entries past offsets[E] written"
+        assert np.array_equal(inv, i_ref), f"call {call}"
         for g, r in zip(got, ref):
             assert torch.equal(g, r), f"call {call}"
-        assert int(st.item()) == 0
+        if st is not None:
+            assert int(st.item()) == 0
 
 
 def test_noalloc_permute_reports_bad_index(B):
