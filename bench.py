@@ -1,25 +1,35 @@
 #!/usr/bin/env python
 """Benchmark of the MoE expert layer (moe_forward) on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-                    [--weights fp4|bfp8]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--only]
+                    [--impl ours|reference] [--weights fp4|bfp8]
 
 One step = one moe_forward (activation cast, routing, counting-sort permute,
 GEMM1 + SwiGLU (.) weight + FP8 requantisation, GEMM2, combine) over the
-workload's T tokens, replayed from a CUDA graph.  Default workload: the
-small-expert decode (T=8, H=2048, I=512, E=256, top-8).  Inputs are seeded
-synthetic tensors (workloads/), resident in HBM when timing starts.  L2 is
-flushed between timed steps (512 MiB written, then 512 MiB read, so no dirty
-flush lines are written back inside the timed step).  Each step is bracketed
-by CUDA events on the launching stream; the timed region is bracketed by a
-barrier and torch.cuda.synchronize().
+workload's T tokens, replayed from a CUDA graph.  The headline workload
+(--workload, default: the skewed prefill, T=8192, H=7168, I=2048, E=256,
+top-8, the largest configuration) gives `value`; the other four workloads
+follow under `per_workload` (--only skips them).  Inputs are seeded synthetic
+tensors (workloads/), resident in HBM when timing starts.  L2 is flushed
+between timed steps (512 MiB written, then 512 MiB read, so no dirty flush
+lines are written back inside the timed step).  Each step is bracketed by CUDA
+events on the launching stream; the headline's timed region is bracketed by
+a barrier and torch.cuda.synchronize(), with nvidia-smi sampling the clocks.
+
+`roofline` describes the layer's dominant GEMM launch, timed alone on the
+state a whole-layer call left (moe_forward's `phases`): the single launch of
+GEMM1 + GEMM2 + combine for small problems, else the longer of the GEMM1 and
+GEMM2 launches.
 
 Multi-GPU: the layer does not shard across GPUs here (replicas only): with N
 ranks each GPU runs its own independent replica, value = all ranks' tokens /
 max-over-ranks time, "scaling": "weak".
 
---impl reference times the CPU oracle (oracle/, float64) on this host's cores
-on a fixed 2-token sample of the same workload (rank 0 only).
+`cpu_baseline` times the CPU oracle (oracle/, float64) on this host's cores on
+a bounded sample: one token for the large workloads, every token of the small
+decode.  --impl reference times the oracle alone as the reference arm (rank 0
+only): one token per step for small workloads, one (token, slot) pair per step
+for the large ones.
 
 --weights bfp8 times the block-FP8 variant instead (moe_forward_bfp8: E4M3
 weights with 128 x 128 block scales, per-128 token scales), on the same
@@ -69,7 +79,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="small_decode")
+    ap.add_argument("--workload", default="skewed_prefill")
+    ap.add_argument("--only", action="store_true", help="measure only --workload (no per_workload entries)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--weights", default="fp4", choices=["fp4", "bfp8"],
@@ -197,6 +208,11 @@ def algorithmic(wl, counts):
         "gemm1_flops": 2 * P * 2 * wl.I * wl.H,
         "gemm2_bytes": touched * w2 + h_q + y_pairs,
         "gemm2_flops": 2 * P * wl.H * wl.I,
+        # GEMM1 + GEMM2 + combine in one launch: h and the per-pair rows stay on
+        # chip / in L2, so the launch's algorithmic bytes are the weights, the
+        # cast tokens and y
+        "fused_bytes": touched * (w1 + w2) + x_q + wl.T * wl.H * 2,
+        "fused_flops": 2 * P * 3 * wl.H * wl.I,
     }
 
 
@@ -250,18 +266,53 @@ def replica_tokens_per_s(world, tokens, steps, total_ms):
 
 # ---------------------------------------------------------------- our arm
 
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+ALL_WORKLOADS = ("tiny", "small_decode", "large_decode", "prefill", "skewed_prefill")
+
+
+def timed_loop(stream, step_fn, steps, flush=None, pre=None):
+    """CUDA-event time (ms) of each of `steps` calls of step_fn on `stream`;
+    before each: flush (L2) and pre (untimed set-up), outside the events."""
+    import torch
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            if flush:
+                flush()
+            if pre:
+                pre()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step_fn()
+            b.record(stream)
+            evs.append((a, b))
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline_of(alg, key, ms, hbm, fp8_peak_tflops):
+    """Roofline entry of one launch: algorithmic bytes and flops of `key`
+    against the measured copy bandwidth / FP8 rate, whichever bound is higher."""
+    nbytes, flops = alg[f"{key}_bytes"], alg[f"{key}_flops"]
+    if nbytes / (hbm * 1e9) >= flops / (fp8_peak_tflops * 1e12):
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": fp8_peak_tflops, "unit": "TFLOP/s",
+            "frac": round(achieved / fp8_peak_tflops, 4), "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
+
+
+def measure(args, wl, dev, stream, world, rank, headline):
+    """One workload: weights, the layer replayed from a CUDA graph (timed), its
+    GEMM launch(es) timed alone, the roofline; for the headline also the
+    clocks, the end-to-end leg and the CPU baseline."""
     import torch
 
     import workloads as W
     from moe_expert_layer_counting_gb300 import binding as B
     from moe_expert_layer_counting_gb300.layer import QuantizedExperts
 
-    wl = W.WORKLOADS.get(args.workload) or W.PROFILE_WORKLOADS[args.workload]
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream(dev)
     x_cpu, logits_cpu = W.tokens(wl)
     x = x_cpu.to(dev)
     logits = logits_cpu.to(dev)
@@ -294,13 +345,14 @@ def run_ours(args, rank, world, local_rank):
     flush_r = torch.ones(128 << 20, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
 
-    def forward(st):
+    def forward(st, phases=0):
         if bfp8:
             B.moe_forward_bfp8(x, logits, w1q, w1s, w2q, w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
-                               counts_out=counts, offsets_out=offsets, perm_out=perm, stream=st)
+                               counts_out=counts, offsets_out=offsets, perm_out=perm, phases=phases, stream=st)
         else:
             B.moe_forward(x, logits, qe.w1q, qe.w1s, qe.w2q, qe.w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
-                          counts_out=counts, offsets_out=offsets, perm_out=perm, tile_n=args.tile_n, stream=st)
+                          counts_out=counts, offsets_out=offsets, perm_out=perm, tile_n=args.tile_n,
+                          phases=phases, stream=st)
 
     def flush():
         if not args.no_flush:
@@ -316,122 +368,78 @@ def run_ours(args, rank, world, local_rank):
         forward(torch.cuda.current_stream())
     counts_np = counts.cpu().numpy()
     n_launch_forward = launches_per_forward_bfp8(T, H, E, k) if bfp8 else launches_per_forward(T, H, E, k)
-
-    def timed_loop(step_fn, steps):
-        evs = []
-        with torch.cuda.stream(stream):
-            for _ in range(steps):
-                flush()
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                step_fn()
-                b.record(stream)
-                evs.append((a, b))
-        stream.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
+    fused = (not bfp8) and n_launch_forward == 2            # GEMM1 + GEMM2 + combine in one launch
+    loop = lambda fn, n, **kw: timed_loop(stream, fn, n, flush=flush, **kw)  # noqa: E731
 
     if args.launch_list:
-        timed_loop(graph.replay, args.warmup + args.steps)
+        loop(graph.replay, args.warmup + args.steps)
+        # then one launch of the layer's GEMM launch(es) alone (the kernels the roofline figures describe)
+        with torch.cuda.stream(stream):
+            if fused:
+                forward(stream, B.PHASE_RESET)
+                forward(stream, B.PHASE_GEMM1 | B.PHASE_GEMM2)
+            else:
+                forward(stream, B.PHASE_GEMM1)
+                forward(stream, B.PHASE_GEMM2)
         torch.cuda.synchronize()
-    else:
-        # warm-up, then a short soak so that the clock sampler sees the GPU under load
-        timed_loop(graph.replay, args.warmup)
+        return {"launch_list": True, "workload": wl.describe(), "replays": args.warmup + args.steps}
+
+    loop(graph.replay, args.warmup)
+    clk = None
+    if headline:
+        # a short soak so that the clock sampler sees the GPU under load, then
+        # the timed region bracketed by a barrier and a device synchronisation
         if world > 1:
             torch.distributed.barrier()
         with ClockSampler(gpu_id_for(dev)) as clk:
             t_soak = time.time()
             while time.time() - t_soak < 1.5:
-                timed_loop(graph.replay, 20)
+                loop(graph.replay, 20)
             if world > 1:
                 torch.distributed.barrier()
             torch.cuda.synchronize()
             t0 = time.time()
-            times = timed_loop(graph.replay, args.steps)
+            times = loop(graph.replay, args.steps)
             torch.cuda.synchronize()
             wall = time.time() - t0
             if world > 1:
                 torch.distributed.barrier()
-        assert B.moe_get_device_status(ws, stream) == 0, "device status word reports an error"
         total_ms, mean_ms = max_over_ranks([sum(times), sum(times) / len(times)], world, dev)
-        value = replica_tokens_per_s(world, T, args.steps, total_ms)
-
-    # per-GEMM timing (dominant kernel) with the layer's own routing
-    if bfp8:
-        ews = ws                              # the GEMMs re-run on the state the forward left
-
-        def phase(ph):
-            B.moe_forward_bfp8(x, logits, w1q, w1s, w2q, w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
-                               counts_out=counts, offsets_out=offsets, perm_out=perm, phases=ph, stream=stream)
     else:
-        ews = torch.empty(B.moe_expert_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
-        xq = torch.empty(T, H, dtype=torch.uint8, device=dev)
-        xs = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
-        y_pairs = torch.empty(k, T, H, dtype=torch.bfloat16, device=dev)
-        with torch.cuda.stream(stream):
-            B.mxq_quantize_act(x, xq, xs, stream=stream)
+        times = loop(graph.replay, args.steps)
+        total_ms, mean_ms = sum(times), sum(times) / len(times)
+    assert B.moe_get_device_status(ws, stream) == 0, "device status word reports an error"
+    value = replica_tokens_per_s(world if headline else 1, T, args.steps, total_ms)
 
-        def phase(ph):
-            B.moe_expert_forward(xq, xs, qe.w1q, qe.w1s, qe.w2q, qe.w2s, idx, wts, counts, offsets, perm, y_pairs,
-                                 ews, tile_n=args.tile_n, phases=ph, stream=stream)
-
-        with torch.cuda.stream(stream):
-            phase(B.PHASE_TOKEN_SCALES | B.PHASE_GEMM1 | B.PHASE_GEMM2)
-    stream.synchronize()
-    if args.launch_list:
-        # after the forward replays: one launch of each GEMM phase alone (the
-        # kernels the roofline figures describe)
-        with torch.cuda.stream(stream):
-            phase(B.PHASE_GEMM1)
-            phase(B.PHASE_GEMM2)
-        torch.cuda.synchronize()
-        return {"launch_list": True, "workload": wl.describe(), "replays": args.warmup + args.steps}
-    g1 = timed_loop(lambda: phase(B.PHASE_GEMM1), max(args.steps, 20))
-    g2 = timed_loop(lambda: phase(B.PHASE_GEMM2), max(args.steps, 20))
-    assert B.moe_get_device_status(ews, stream) == 0
-    g1_ms, g2_ms = statistics.mean(g1), statistics.mean(g2)
+    # the layer's GEMM launch(es) alone, on the state the forward left
+    nt = max(args.steps, 20)
+    if fused:
+        g_ms = statistics.mean(loop(lambda: forward(stream, B.PHASE_GEMM1 | B.PHASE_GEMM2), nt,
+                                    pre=lambda: forward(stream, B.PHASE_RESET)))
+        gemm_ms = {"gemm1_gemm2_combine": round(g_ms, 5)}
+    else:
+        g1 = statistics.mean(loop(lambda: forward(stream, B.PHASE_GEMM1), nt))
+        g2 = statistics.mean(loop(lambda: forward(stream, B.PHASE_GEMM2), nt))
+        gemm_ms = {"gemm1": round(g1, 5), "gemm2": round(g2, 5)}
+    assert B.moe_get_device_status(ws, stream) == 0
 
     alg = algorithmic_bfp8(wl, counts_np) if bfp8 else algorithmic(wl, counts_np)
     hbm, bf16, peak_src = peaks()
     fp8_peak_tflops = 2 * bf16                      # FP8 dense = 2x BF16 dense (nominal ratio)
-    dom = "gemm1" if g1_ms >= g2_ms else "gemm2"
-    dom_ms = max(g1_ms, g2_ms)
-    dom_bytes = alg[f"{dom}_bytes"]
-    dom_flops = alg[f"{dom}_flops"]
-    t_bytes = dom_bytes / (hbm * 1e9)
-    t_flops = dom_flops / (fp8_peak_tflops * 1e12)
-    if t_bytes >= t_flops:
-        achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4)}
-    else:
-        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": fp8_peak_tflops, "unit": "TFLOP/s",
-                "frac": round(achieved / fp8_peak_tflops, 4)}
     kname = "bfp8_gemm_kernel" if bfp8 else "expert_gemm_kernel"
-    roof.update({"kernel": f"{kname} ({dom}, one launch)", "ms": round(dom_ms, 5),
-                 "algorithmic_bytes": dom_bytes, "algorithmic_flops": dom_flops,
-                 "traffic": measured_traffic(wl.name, dom, bfp8), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)"})
+    if fused:
+        dom, dom_ms = "fused", g_ms
+        what = f"{kname}<16, GEMM1 + GEMM2 + combine> (one launch)"
+    else:
+        dom = "gemm1" if g1 >= g2 else "gemm2"
+        dom_ms = max(g1, g2)
+        what = f"{kname} ({dom}, one launch)"
+    roof = roofline_of(alg, dom, dom_ms, hbm, fp8_peak_tflops)
+    roof.update({"kernel": what, "ms": round(dom_ms, 5), "traffic": measured_traffic(wl.name, dom, bfp8),
+                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)"})
     layer_time_bound = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (fp8_peak_tflops * 1e12))
-    # context for the fraction: PyTorch kernels moving the same number of DRAM
-    # bytes as the dominant kernel, cold L2 like the kernel -- a copy (half the
-    # bytes read, half written) and a read-only reduction (sum)
-    half = max(dom_bytes // 8, 1)                   # float32 elements in half the bytes
-    cp_src = torch.ones(half, dtype=torch.float32, device=dev)
-    cp_dst = torch.empty_like(cp_src)
-    copy_ms = statistics.median(timed_loop(lambda: cp_dst.copy_(cp_src), max(args.steps, 20)))
-    del cp_src, cp_dst
-    read_buf = torch.ones(max(dom_bytes // 4, 1), dtype=torch.float32, device=dev)
-    read_out = torch.empty((), dtype=torch.float32, device=dev)
-    read_ms = statistics.median(timed_loop(lambda: torch.sum(read_buf, dim=(0,), out=read_out), max(args.steps, 20)))
-    del read_buf
-
-    result = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "fp8xfp8, 128x128 block scales (fp32 accumulate)" if bfp8 else "fp8xfp4 (fp32 accumulate)",
-        "data": "synthetic (seeded, workloads/)",
+    out = {
+        "value": round(value, 1), "ms_per_step": round(mean_ms, 5),
         "config": {"workload": wl.describe() + (" block-FP8 weights" if bfp8 else ""), "tokens_per_step": T,
                    "pairs": T * k, "weights": args.weights + (" (tile-contiguous codes)" if bfp8 else ""),
                    "touched_experts": alg["touched_experts"], "tile_n": args.tile_n or "auto",
@@ -439,120 +447,245 @@ def run_ours(args, rank, world, local_rank):
                    "cuda_graph": True, "parallelism": "replicas" if world > 1 else "single GPU"},
         "layer_roofline_frac": round(layer_time_bound / (mean_ms * 1e-3), 4),
         "layer_rates": layer_rates(alg, mean_ms),
-        "gemm_ms": {"gemm1": round(g1_ms, 5), "gemm2": round(g2_ms, 5)},
+        "gemm_ms": gemm_ms,
         "roofline": roof,
-        "same_size_reference": {"bytes": dom_bytes,
-                                "copy_ms": round(copy_ms, 5), "copy_gbs": round(dom_bytes / (copy_ms * 1e-3) / 1e9, 1),
-                                "sum_ms": round(read_ms, 5), "sum_gbs": round(dom_bytes / (read_ms * 1e-3) / 1e9, 1),
-                                "what": "PyTorch copy_ of bytes/2 (bytes of DRAM traffic) and torch.sum over bytes, "
-                                        "float32, L2 flushed before each call (median)"},
         "gpu_launches": n_launch_forward * args.steps,
-        "wall_s_timed_region": round(wall, 4),
-        "clocks": clk.summary(),
     }
+    if headline:
+        # context for the fraction: PyTorch kernels moving the same number of DRAM
+        # bytes as the dominant kernel, cold L2 like the kernel -- a copy (half the
+        # bytes read, half written) and a read-only reduction (sum)
+        dom_bytes = roof["algorithmic_bytes"]
+        half = max(dom_bytes // 8, 1)                   # float32 elements in half the bytes
+        cp_src = torch.ones(half, dtype=torch.float32, device=dev)
+        cp_dst = torch.empty_like(cp_src)
+        copy_ms = statistics.median(loop(lambda: cp_dst.copy_(cp_src), nt))
+        del cp_src, cp_dst
+        read_buf = torch.ones(max(dom_bytes // 4, 1), dtype=torch.float32, device=dev)
+        read_out = torch.empty((), dtype=torch.float32, device=dev)
+        read_ms = statistics.median(loop(lambda: torch.sum(read_buf, dim=(0,), out=read_out), nt))
+        del read_buf
+        out["same_size_reference"] = {
+            "bytes": dom_bytes, "copy_ms": round(copy_ms, 5),
+            "copy_gbs": round(dom_bytes / (copy_ms * 1e-3) / 1e9, 1), "sum_ms": round(read_ms, 5),
+            "sum_gbs": round(dom_bytes / (read_ms * 1e-3) / 1e9, 1),
+            "what": "PyTorch copy_ of bytes/2 (bytes of DRAM traffic) and torch.sum over bytes, float32, "
+                    "L2 flushed before each call (median)"}
+        out["wall_s_timed_region"] = round(wall, 4)
+        out["clocks"] = clk.summary()
+        if not args.quick:
+            # end to end through the public API with host buffers: H2D inputs, layer, D2H output
+            x_h = x_cpu.pin_memory()
+            l_h = logits_cpu.pin_memory()
+            y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
 
-    if not args.quick:
-        # end to end through the public API with host buffers: H2D inputs, layer, D2H output
-        x_h = x_cpu.pin_memory()
-        l_h = logits_cpu.pin_memory()
-        y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+            def e2e_step():
+                x.copy_(x_h, non_blocking=True)
+                logits.copy_(l_h, non_blocking=True)
+                graph.replay()
+                y_h.copy_(y, non_blocking=True)
 
-        def e2e_step():
-            x.copy_(x_h, non_blocking=True)
-            logits.copy_(l_h, non_blocking=True)
-            graph.replay()
-            y_h.copy_(y, non_blocking=True)
+            e2e_times = loop(e2e_step, args.steps)
+            e2e_total = max_over_ranks([sum(e2e_times)], world, dev)[0]
+            out["e2e"] = {"value": round(replica_tokens_per_s(world, T, args.steps, e2e_total), 1), "unit": UNIT,
+                          "h2d_bytes_per_step": x_h.numel() * 2 + l_h.numel() * 4,
+                          "d2h_bytes_per_step": y_h.numel() * 2}
+    del graph
+    return out
 
-        e2e_times = timed_loop(e2e_step, args.steps)
-        e2e_total = max_over_ranks([sum(e2e_times)], world, dev)[0]
-        result["e2e"] = {"value": round(replica_tokens_per_s(world, T, args.steps, e2e_total), 1), "unit": UNIT,
-                         "h2d_bytes_per_step": x_h.numel() * 2 + l_h.numel() * 4,
-                         "d2h_bytes_per_step": y_h.numel() * 2}
-        if rank == 0 and world == 1:
-            result["cpu_baseline"] = cpu_baseline(wl, steps=2, bfp8=bfp8)
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import workloads as W
+    wl = W.WORKLOADS.get(args.workload) or W.PROFILE_WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    head = measure(args, wl, dev, stream, world, rank, headline=True)
+    if args.launch_list:
+        return head
+    result = {"metric": METRIC, "value": head.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+              "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"), "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None,
+              "dtype": "fp8xfp8, 128x128 block scales (fp32 accumulate)" if args.weights == "bfp8"
+              else "fp8xfp4 (fp32 accumulate)",
+              "data": "synthetic (seeded, workloads/)"}
+    result.update(head)
+    torch.cuda.empty_cache()
+    if not args.quick and rank == 0 and world == 1:
+        result["cpu_baseline"] = cpu_baseline(wl, bfp8=args.weights == "bfp8")
+    if not args.only and args.workload in ALL_WORKLOADS:
+        per = {}
+        for name in ALL_WORKLOADS:
+            if name == args.workload:
+                continue
+            other = measure(args, W.WORKLOADS[name], dev, stream, world, rank, headline=False)
+            if name == "small_decode" and not args.quick and rank == 0 and world == 1:
+                other["cpu_baseline"] = cpu_baseline(W.WORKLOADS[name], bfp8=args.weights == "bfp8")
+            per[name] = other
+            torch.cuda.empty_cache()
+        result["per_workload"] = per
     return result
 
 
 # ---------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(wl, n_tokens=2, bfp8=False):
-    """A fixed token sample of the workload and the oracle-quantised experts it needs."""
+def _spawn_pool():
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    return cf.ProcessPoolExecutor(max_workers=max(1, min(16, len(os.sched_getaffinity(0)))),
+                                  mp_context=mp.get_context("spawn"))
+
+
+def _oracle_weights(wl, experts, bfp8):
+    """The oracle's quantised weights of `experts` (untimed set-up), in arrays
+    over all E experts (untouched experts stay zero, never read)."""
     import numpy as np
     import torch
 
     import workloads as W
     from oracle import bfp8 as OB
     from oracle import moe as O
-    x, logits = W.tokens(wl)
-    idx, _ = O.route_topk(logits[:n_tokens].numpy(), wl.k)
-    need = sorted(set(idx.reshape(-1).tolist()))
     E, H, I = wl.E, wl.H, wl.I
     if bfp8:
         quant = OB.quantize_weight
-        w1q = np.zeros((E, 2 * I, H), np.uint8); w1s = np.zeros((E, 2 * I // 128, H // 128), np.float32)
-        w2q = np.zeros((E, H, I), np.uint8); w2s = np.zeros((E, H // 128, I // 128), np.float32)
+        w = [np.zeros((E, 2 * I, H), np.uint8), np.zeros((E, 2 * I // 128, H // 128), np.float32),
+             np.zeros((E, H, I), np.uint8), np.zeros((E, H // 128, I // 128), np.float32)]
     else:
         quant = O.quantize_weight
-        w1q = np.zeros((E, 2 * I, H // 2), np.uint8); w1s = np.zeros((E, 2 * I, H // 32), np.uint8)
-        w2q = np.zeros((E, H, I // 2), np.uint8); w2s = np.zeros((E, H, I // 32), np.uint8)
-    for e in need:
-        l1, l2 = W.expert_weights(wl, e, "cpu")
-        q, s = quant(l1.view(torch.int16).numpy().view(np.uint16)[None])
-        w1q[e], w1s[e] = q[0], s[0]
-        q, s = quant(l2.view(torch.int16).numpy().view(np.uint16)[None])
-        w2q[e], w2s[e] = q[0], s[0]
+        w = [np.zeros((E, 2 * I, H // 2), np.uint8), np.zeros((E, 2 * I, H // 32), np.uint8),
+             np.zeros((E, H, I // 2), np.uint8), np.zeros((E, H, I // 32), np.uint8)]
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)[None]  # noqa: E731
+    big = len(experts) > 2 and 3 * H * I > (1 << 22)
+    pool = _spawn_pool() if big else None
+    try:
+        jobs = []
+        for e in experts:
+            l1, l2 = W.expert_weights(wl, e, "cpu")
+            if pool:
+                jobs.append((e, pool.submit(quant, bits(l1)), pool.submit(quant, bits(l2))))
+            else:
+                jobs.append((e, quant(bits(l1)), quant(bits(l2))))
+        for e, r1, r2 in jobs:
+            (q1, s1), (q2, s2) = (r1.result(), r2.result()) if pool else (r1, r2)
+            w[0][e], w[1][e], w[2][e], w[3][e] = q1[0], s1[0], q2[0], s2[0]
+    finally:
+        if pool:
+            pool.shutdown()
+    return w
+
+
+def _oracle_sample(wl, n_tokens, bfp8):
+    """The first `n_tokens` tokens of the workload and the oracle-quantised
+    weights of the experts they route to."""
+    import numpy as np
+    import torch
+
+    import workloads as W
+    from oracle import moe as O
+    x, logits = W.tokens(wl)
+    idx, _ = O.route_topk(logits[:n_tokens].numpy(), wl.k)
+    need = sorted(set(idx.reshape(-1).tolist()))
     xb = x[:n_tokens].view(torch.int16).numpy().view(np.uint16)
-    return xb, logits[:n_tokens].numpy(), (w1q, w1s, w2q, w2s), bfp8
+    return xb, logits[:n_tokens].numpy(), _oracle_weights(wl, need, bfp8), bfp8
 
 
-def _oracle_step(wl, sample):
+def _oracle_tokens_step(wl, sample):
+    """One step of the CPU baseline: the oracle's whole layer on the sample's tokens."""
     from oracle import bfp8 as OB
     from oracle import moe as O
     xb, lg, w, bfp8 = sample
     (OB if bfp8 else O).forward(xb, lg, *w, wl.k)
 
 
-def cpu_baseline(wl, steps=2, n_tokens=2, bfp8=False):
+def _heavy(wl):
+    """Per-token oracle cost is tens of seconds: sample pairs, not tokens."""
+    return 3 * wl.H * wl.I > (1 << 24)
+
+
+def cpu_baseline(wl, bfp8=False, steps=None):
+    """The oracle timed on this host's cores (BLAS threads: all of them) on a
+    bounded sample of the workload: every token for the small workloads,
+    one token (its k experts) for the large ones."""
+    n_tokens = 1 if _heavy(wl) else wl.T
+    steps = steps or (1 if _heavy(wl) else 2)
     sample = _oracle_sample(wl, n_tokens, bfp8)
-    _oracle_step(wl, sample)
+    if not _heavy(wl):
+        _oracle_tokens_step(wl, sample)            # warm-up
     t0 = time.time()
     for _ in range(steps):
-        _oracle_step(wl, sample)
+        _oracle_tokens_step(wl, sample)
     dt = (time.time() - t0) / steps
     what = "block-FP8 oracle" if bfp8 else "oracle"
-    return {"value": round(n_tokens / dt, 3), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+    full = "all" if n_tokens == wl.T else f"the first {n_tokens}"
+    return {"value": round(n_tokens / dt, 4), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
-            "sample": f"{n_tokens} tokens of {wl.describe()} ({n_tokens * wl.k} pairs) per step, float64 "
-                      f"NumPy {what} (weights of the experts they route to quantised untimed), {steps} steps"}
+            "sample": f"{full} token(s) of {wl.describe()} ({n_tokens * wl.k} pairs) per step through the "
+                      f"float64 NumPy {what}'s whole layer (weights of the experts they route to quantised "
+                      f"untimed), {steps} step(s), {dt:.2f} s per step"}
 
 
 def run_reference(args):
+    """The reference arm: the oracle, as it stands, on this host's cores.
+    Small workloads: one token through the oracle's whole layer per step.
+    Large workloads (a token costs tens of seconds): one (token, slot) pair per
+    step through the oracle's expert GEMMs (GEMM1 + SwiGLU + requantisation +
+    GEMM2), i.e. 1/k token of work, with the token's cast and routing done
+    once, untimed (microseconds at one token)."""
+    import numpy as np
+
     import workloads as W
-    wl = W.WORKLOADS[args.workload]
-    n_tokens = 2
+    from oracle import bfp8 as OB
+    from oracle import moe as O
+    wl = W.WORKLOADS.get(args.workload) or W.PROFILE_WORKLOADS[args.workload]
     bfp8 = args.weights == "bfp8"
-    sample = _oracle_sample(wl, n_tokens, bfp8)
+    M = OB if bfp8 else O
+    if _heavy(wl):
+        x, logits = W.tokens(wl)
+        import torch
+        xb = x[:1].view(torch.int16).numpy().view(np.uint16)
+        idx, w = M.route_topk(logits[:1].numpy(), wl.k)
+        e = int(idx[0, 0])
+        one = np.full_like(idx, -1)
+        one[0, 0] = e
+        weights = _oracle_weights(wl, [e], bfp8)
+        xq, xs = M.quantize_act(xb)
+
+        def step():
+            M.expert_forward(xq, xs, *weights, one, w, wl.E, experts=[e])
+        tokens_per_step = 1.0 / wl.k
+        sample_txt = (f"one (token, slot) pair of {wl.describe()} per step (1/{wl.k} token): the float64 NumPy "
+                      f"{'block-FP8 ' if bfp8 else ''}oracle's expert GEMMs for that pair (expert {e}); weights "
+                      f"quantised, token cast and routed once, untimed")
+    else:
+        sample = _oracle_sample(wl, 1, bfp8)
+
+        def step():
+            _oracle_tokens_step(wl, sample)
+        tokens_per_step = 1.0
+        sample_txt = (f"one token of {wl.describe()} per step through the float64 NumPy "
+                      f"{'block-FP8 ' if bfp8 else ''}oracle's whole layer (weights of its experts quantised "
+                      f"untimed)")
     for _ in range(args.warmup):
-        _oracle_step(wl, sample)
+        step()
     times = []
     for _ in range(args.steps):
         t0 = time.time()
-        _oracle_step(wl, sample)
+        step()
         times.append(time.time() - t0)
     total = sum(times)
-    value = n_tokens * args.steps / total
+    value = tokens_per_step * args.steps / total
     cores = len(os.sched_getaffinity(0))
-    sample_txt = (f"{n_tokens} tokens of {wl.describe()} ({n_tokens * wl.k} pairs) per step, float64 NumPy "
-                  f"{'block-FP8 ' if bfp8 else ''}oracle, weights of the routed experts quantised untimed")
-    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, workloads/)",
             "config": {"workload": wl.describe() + (" block-FP8 weights" if bfp8 else ""),
-                       "tokens_per_step": n_tokens, "weights": args.weights},
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                       "tokens_per_step": tokens_per_step, "weights": args.weights},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample_txt},
-            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def launches_per_forward(T, H, E, k):

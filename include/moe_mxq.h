@@ -196,7 +196,8 @@ enum moe_phase {
     MOE_PHASE_TOKEN_SCALES = 1,
     MOE_PHASE_GEMM1 = 2,
     MOE_PHASE_GEMM2 = 4,
-    MOE_PHASE_H_SCALES = 8
+    MOE_PHASE_H_SCALES = 8,
+    MOE_PHASE_RESET = 16      /* moe_forward only: zero the status words and arrival counters */
 };
 
 typedef struct moe_expert_args {
@@ -248,6 +249,19 @@ typedef struct moe_forward_args {
     void *workspace;
     size_t workspace_bytes;
     int32_t route_mode;     /* enum moe_route_mode; 0 = softmax, renormalised */
+    /* 0: the whole layer.  Otherwise a mask of enum moe_phase, for timing the
+     * expert GEMMs alone on the state that an earlier whole-layer call with
+     * the same arguments left in the workspace:
+     *   MOE_PHASE_RESET zeroes the status words and arrival counters (the
+     *     first thing a whole-layer call does);
+     *   MOE_PHASE_GEMM1 / MOE_PHASE_GEMM2 re-run the layer's GEMM launches
+     *     (the same kernels and launch shapes as the whole-layer call); where
+     *     the layer runs GEMM1, GEMM2 and the combine in one launch, both bits
+     *     are required together, that launch also writes y, and its arrival
+     *     counters must have been zeroed (RESET, in this call or an earlier one).
+     * RESET runs before the GEMMs when combined.  Routing, permute and the
+     * activation cast are not re-run.  Other bits: MOE_ERR_INVALID_ARG. */
+    int32_t phases;
 } moe_forward_args;
 
 MOE_API size_t moe_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k);

@@ -109,6 +109,8 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   if (!a || a->struct_size != sizeof(moe_forward_args)) return MOE_ERR_INVALID_ARG;
   if (a->T < 0 || a->H <= 0 || a->I <= 0 || a->E <= 0 || a->k <= 0) return MOE_ERR_INVALID_ARG;
   if (!route_mode_valid(a->route_mode)) return MOE_ERR_INVALID_ARG;
+  const int phases = a->phases;
+  if (phases & ~(MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2 | MOE_PHASE_RESET)) return MOE_ERR_INVALID_ARG;
   if (!a->workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(a->workspace, 256)) return MOE_ERR_MISALIGNED;
   const ForwardWs lay = forward_ws_layout(a->T, a->H, a->I, a->E, a->k);
@@ -141,22 +143,36 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
       return MOE_ERR_MISALIGNED;
   }
 
-  if (cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // phases != 0: timing / isolation, only the layer's GEMM launch(es) on the
+  // state an earlier whole-layer call left in the workspace
+  const int gemms = phases & (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2);
+  const int64_t P = a->T * a->k;
+  ea.tile_n = a->tile_n ? a->tile_n : choose_tile_n(P, a->E);
+  const bool fused = a->T > 0 && front_eligible(a->T, a->H, a->E, a->k) &&
+                     fused_eligible(a->T, a->H, a->E, a->k, ea.tile_n);
+  if (fused && gemms != 0 && gemms != (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2)) return MOE_ERR_INVALID_ARG;
+
+  if ((phases == 0 || (phases & MOE_PHASE_RESET)) && cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (phases != 0) {
+    if (gemms == 0 || a->T == 0) return MOE_OK;
+    if (fused) return launch_fused_gemms(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
+    ea.phases = gemms;
+    return launch_expert_forward(&ea, status, ws + lay.expert, st);
+  }
   if (a->T == 0) {
     if (a->counts_out && cudaMemsetAsync(a->counts_out, 0, (size_t)a->E * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (a->offsets_out && cudaMemsetAsync(a->offsets_out, 0, (size_t)(a->E + 1) * 4, st) != cudaSuccess)
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  const int64_t P = a->T * a->k;
-  ea.tile_n = a->tile_n ? a->tile_n : choose_tile_n(P, a->E);
   int32_t *inv_perm = reinterpret_cast<int32_t *>(ws + lay.inv_perm);
   if (front_eligible(a->T, a->H, a->E, a->k)) {
     // small problems: routing + permute + pool cast in one launch
     rc = launch_front(&ea, a->x, a->logits, a->route_mode, idx, wts, inv_perm, ws + lay.expert, st);
     if (rc != MOE_OK) return rc;
     // then, with 16-token tiles, both GEMMs and the combine in one more
-    if (fused_eligible(a->T, a->H, a->E, a->k, ea.tile_n))
+    if (fused)
       return launch_fused_gemms(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
     ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
     rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
