@@ -57,7 +57,7 @@ METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM G
 # built from sources whose SHA-256 is `src_sha256`
 # (commands and figures in profiles/).  `traffic` is reported as null once
 # those sources change.
-GEMM_SOURCES = ("gemm.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
+GEMM_SOURCES = ("gemm.cu", "gemm2sm.cu", "gemm_common.cuh", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC = {
     "src_sha256": "34049e5ab0ee6b69086c8a0d5539f70af5e8ef42ab113637067f39a5008b6996",
     "small_decode": {"gemm1": 62794496 + 2048, "gemm2": 31327744 + 0},

@@ -182,7 +182,10 @@ MOE_API int moe_permute_noalloc(const int32_t *topk_idx, int64_t T, int32_t E, i
  *            Rows of dropped pairs are not written.
  *   hq/hs: optional outputs (NULL = not written): the requantised h in pool
  *          order, hq [P][I] e4m3 and hs [P][I/32] ue8m0, row s = pair perm[s].
- *   tile_n: token tile (16, 32, 64, 128) or 0 to let the library choose.
+ *   tile_n: token tile (16, 32, 64, 128, 208, 224) or 0 to let the library
+ *          choose.  208 and 224 both mean the large tile: 208 tokens with the
+ *          GEMMs on CTA pairs where both GEMMs' 128-row weight tiles pair up
+ *          (2I/128 and H/128 even), 224 tokens on single CTAs otherwise.
  *   phases: 0 for the whole layer, or a mask of enum moe_phase to run steps
  *          separately on the same workspace (same tile_n in every call):
  *          TOKEN_SCALES gathers GEMM1's token scales into the workspace;

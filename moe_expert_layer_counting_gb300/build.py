@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_mxq.so")
-SOURCES = ["quant.cu", "route.cu", "permute.cu", "permute_noalloc.cu", "gemm.cu", "combine.cu", "api.cu", "bfp8.cu"]
+SOURCES = ["quant.cu", "route.cu", "permute.cu", "permute_noalloc.cu", "gemm.cu", "gemm2sm.cu", "combine.cu", "api.cu", "bfp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -147,7 +147,7 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   // state an earlier whole-layer call left in the workspace
   const int gemms = phases & (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2);
   const int64_t P = a->T * a->k;
-  ea.tile_n = a->tile_n ? a->tile_n : choose_tile_n(P, a->E);
+  ea.tile_n = resolve_tile_n(a->tile_n, P, a->E, a->H, a->I);
   const bool fused = a->T > 0 && front_eligible(a->T, a->H, a->E, a->k) &&
                      fused_eligible(a->T, a->H, a->E, a->k, ea.tile_n);
   if (fused && gemms != 0 && gemms != (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2)) return MOE_ERR_INVALID_ARG;

@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <cstdlib>
 
+#include "gemm_common.cuh"
 #include "host_common.h"
 #include "layer_blocks.cuh"
 #include "ptx.cuh"
@@ -46,15 +47,6 @@
 namespace mxq {
 
 namespace {
-
-constexpr int kBM = 128;
-constexpr int kBK = 128;
-constexpr int kChunk = 16;                    // accumulator columns per epilogue step
-constexpr long long kWaitLimit = 2000000000LL;
-constexpr long long kInjectedWaitLimit = 20000000LL;   // ~10 ms: the debug wait's budget
-constexpr int kMaxE = 1024;
-constexpr int kWTileBytes = kBM * kBK / 2;    // one packed FP4 weight tile in HBM (8 KB)
-constexpr int kPrefetchAhead = 2;             // K blocks between an L2 prefetch and its TMA load
 
 // Issue cost.  Every asynchronous instruction (TMA copy, tcgen05.cp,
 // tcgen05.mma) takes ~80 cycles of its issuing thread, whatever its size,
@@ -150,64 +142,7 @@ struct GemmArgs {
   uint4 *y;                         // [T][H] bf16 (combine output)
 };
 
-struct TileInfo {
-  int e, mt, g, s0, valid;
-};
 
-// counts/offsets -> shared memory with independent loads by every thread of
-// the block (no chain of dependent global loads in the prologue).
-__device__ __forceinline__ void load_expert_table(const int32_t *counts, const int32_t *offsets, int E,
-                                                  int *cnt_sm, int *off_sm, bool from_l2 = false) {
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    if (from_l2) {
-      if (e < E) cnt_sm[e] = __ldcg(counts + e);
-      off_sm[e] = __ldcg(offsets + e);
-    } else {
-      if (e < E) cnt_sm[e] = __ldg(counts + e);
-      off_sm[e] = __ldg(offsets + e);
-    }
-  }
-}
-
-template <int BN>
-__device__ __forceinline__ TileInfo decode_work(int w, int MT, int E, const int *tile_off, const int *cnt_sm,
-                                                const int *off_sm) {
-  const int tq = w / MT;
-  int lo = 0, hi = E;                // find e with tile_off[e] <= tq < tile_off[e+1]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tile_off[mid] <= tq) lo = mid; else hi = mid;
-  }
-  TileInfo ti;
-  ti.e = lo;
-  const int nte = tile_off[lo + 1] - tile_off[lo];
-  const int local = w - tile_off[lo] * MT;
-  ti.mt = local / nte;
-  const int nt = local - ti.mt * nte;
-  ti.g = tile_off[lo] + nt;
-  ti.s0 = off_sm[lo] + nt * BN;
-  const int rem = cnt_sm[lo] - nt * BN;
-  ti.valid = rem < BN ? rem : BN;
-  return ti;
-}
-
-// Optional wait-time accounting (build with -DMOE_MXQ_WAIT_STATS): each role
-// adds the clock cycles it spent in bounded waits, and its total, to 64-bit
-// counters at byte 64 of the status area: [0] producer on empty stages,
-// [1] MMA on full stages, [2] MMA on free accumulators, [3] epilogue on full
-// accumulators, [4] kernel cycles of warp 0, [5] kernel cycles of warp 1,
-// [6] kernel cycles of warp 2, [7] work items.
-#ifdef MOE_MXQ_WAIT_STATS
-#define MXQ_TIMED_WAIT(slot, expr)                                   \
-  ([&]() {                                                           \
-    const long long _t0 = clock64();                                 \
-    const bool _r = (expr);                                          \
-    if (lane == 0) wait_acc[slot] += clock64() - _t0;                \
-    return _r;                                                       \
-  }())
-#else
-#define MXQ_TIMED_WAIT(slot, expr) (expr)
-#endif
 
 template <int BN, int PHASE>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
@@ -547,81 +482,12 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
         uint32_t v[16];
         tmem_ld_32x32b_x16(t_row + (uint32_t)c0, v);
         tmem_ld_wait();
-        if (it.l1) {
-          // lane l of quadrant q holds stored row 32q+l: gate when (l & 8) == 0,
-          // the matching up row sits 8 lanes away (8-row gate/up interleave).
-          const bool is_gate = (lane & 8) == 0;
-          const int feat = 16 * q + 8 * (lane >> 4) + (lane & 7);   // tile-local feature 0..63
-          const int jbase = is_gate ? 0 : 8;                         // columns this lane evaluates
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float mine = __uint_as_float(v[j]);
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
-            // columns past the tile's tokens hold no pair and are never stored
-            if (j >= jbase && j < jbase + 8 && c0 + j < ti.valid) {
-              const float g = is_gate ? mine : other;
-              const float u = is_gate ? other : mine;
-              // silu(g) = g / (1 + e^-g); the approximate divide (2 ulp, no
-              // slow path) is far inside the FP8 step of the requantisation
-              const float h = __fdividef(g, 1.0f + __expf(-g)) * u * row_w[c0 + j];
-              ebuf_f[j * 64 + feat] = h;
-            }
-          }
-          named_bar_sync(bar_half, 128);
-          // requantise: 16 columns x 2 groups of 32 features = 32 items; an
-          // 8-lane group takes one item, 4 features per lane (one 16-byte
-          // read, a 3-step xor max, one 4-byte store), 4 items per warp pass
-#pragma unroll
-          for (int pass = 0; pass < 2; ++pass) {
-            const int it = q * 8 + pass * 4 + (lane >> 3);
-            const int col = it >> 1, grp = it & 1;
-            const int c = c0 + col;
-            const int f4 = (lane & 7) * 4;                            // this lane's first feature in the group
-            const float4 hv = *reinterpret_cast<const float4 *>(ebuf_f + col * 64 + grp * 32 + f4);
-            float amax = fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w)));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-            if (c >= ti.valid) continue;                              // uniform in the 8-lane group
-            const int e = ue8m0_exponent<true>(amax);
-            const float inv = pow2_neg(e);
-            const uint32_t codes = (uint32_t)cvt_e4m3x2(hv.x * inv, hv.y * inv) |
-                                   ((uint32_t)cvt_e4m3x2(hv.z * inv, hv.w * inv) << 16);
-            const size_t s = (size_t)(ti.s0 + c);
-            const int fcol = ti.mt * 64 + grp * 32;                  // first feature of the group
-            *reinterpret_cast<uint32_t *>(args.hq + s * args.I + fcol + f4) = codes;
-            if ((lane & 7) == 0) {
-              const int fg = fcol >> 5;                               // 32-group index along I
-              const size_t chunk = (size_t)ti.g * (args.I / 128) + (fg >> 2);
-              const int cr = c & 127;
-              args.sfb2[chunk * C::kTokChunk + (c >> 7) * 512 + (cr & 31) * 16 + (cr >> 5) * 4 + (fg & 3)] =
-                  (uint8_t)(e + 127);
-              if (args.hs_out) args.hs_out[s * (args.I / 32) + fg] = (uint8_t)(e + 127);
-            }
-          }
-          named_bar_sync(bar_half, 128);
-        } else {
-          const int row = 32 * q + lane;                             // output feature inside the tile
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
-            ebuf_h[j * 128 + row] = *reinterpret_cast<const uint16_t *>(&b);
-          }
-          named_bar_sync(bar_half, 128);
-#pragma unroll
-          for (int it = 0; it < 2; ++it) {
-            const int col = q + 4 * (2 * it + (lane >> 4));
-            const int c = c0 + col;
-            if (c < ti.valid) {
-              const int p = row_pair[c];
-              const int t = p / args.k, j = p - t * args.k;
-              const int l16 = lane & 15;
-              uint16_t *dst = args.y_pairs + ((size_t)j * args.T + t) * args.H + (size_t)ti.mt * kBM + l16 * 8;
-              *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(ebuf_h + col * 128 + l16 * 8);
-            }
-          }
-          named_bar_sync(bar_half, 128);
-        }
+        if (it.l1)
+          epilogue_gemm1_chunk(v, c0, q, lane, ti, row_w, ebuf_f, bar_half, args.I, C::kTokChunk, args.hq,
+                               args.sfb2, args.hs_out);
+        else
+          epilogue_gemm2_chunk(v, c0, q, lane, ti, row_pair, ebuf_h, bar_half, args.k, args.T, args.H,
+                               args.y_pairs);
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
@@ -1024,6 +890,12 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
       launch_prep<BN, false>(a->hs, a, (int)(a->I / 128), sfb2, nullptr, nullptr, nullptr, st) != MOE_OK)
     return MOE_ERR_CUDA;
 
+  if constexpr (BN == 208) {
+    // the large tile on CTA pairs (gemm2sm.cu; resolve_tile_n picks 208 only
+    // where the weight tiles pair up)
+    const int ph = phases & (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2);
+    return ph ? run_expert_pairs(a, ph, status, hq, sfb1, sfb2, w_pool, xq_pool, st) : MOE_OK;
+  } else {
   GemmArgs g{};
   g.E = E; g.k = a->k; g.T = (int)a->T; g.H = (int)a->H; g.I = (int)a->I;
   g.counts = a->counts; g.offsets = a->offsets; g.perm = a->perm;
@@ -1065,6 +937,7 @@ int run_expert(const moe_expert_args *a, int *status, char *ws, const ExpertWs &
       return MOE_ERR_CUDA;
   }
   return MOE_OK;
+  }
 }
 
 }  // namespace
@@ -1073,12 +946,13 @@ int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch,
   const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
   if (a->T == 0) return MOE_OK;
   char *ws = reinterpret_cast<char *>(scratch);
-  const int bn = a->tile_n ? a->tile_n : choose_tile_n(a->T * a->k, a->E);
+  const int bn = resolve_tile_n(a->tile_n, a->T * a->k, a->E, a->H, a->I);
   switch (bn) {
     case 16: return launch_pool_cast_t<16>(a, x, ws, lay, st);
     case 32: return launch_pool_cast_t<32>(a, x, ws, lay, st);
     case 64: return launch_pool_cast_t<64>(a, x, ws, lay, st);
     case 128: return launch_pool_cast_t<128>(a, x, ws, lay, st);
+    case 208: return launch_pool_cast_t<208>(a, x, ws, lay, st);
     case 224: return launch_pool_cast_t<224>(a, x, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
@@ -1092,12 +966,13 @@ int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logit
                  float *wts, int32_t *inv_perm, void *scratch, cudaStream_t st) {
   const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
   char *ws = reinterpret_cast<char *>(scratch);
-  const int bn = a->tile_n ? a->tile_n : choose_tile_n(a->T * a->k, a->E);
+  const int bn = resolve_tile_n(a->tile_n, a->T * a->k, a->E, a->H, a->I);
   switch (bn) {
     case 16: return launch_front_t<16>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
     case 32: return launch_front_t<32>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
     case 64: return launch_front_t<64>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
     case 128: return launch_front_t<128>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
+    case 208: return launch_front_t<208>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
     case 224: return launch_front_t<224>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
@@ -1168,12 +1043,13 @@ int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, 
   const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
   if (a->T == 0) return MOE_OK;
   char *ws = reinterpret_cast<char *>(scratch);
-  const int bn = a->tile_n ? a->tile_n : choose_tile_n(a->T * a->k, a->E);
+  const int bn = resolve_tile_n(a->tile_n, a->T * a->k, a->E, a->H, a->I);
   switch (bn) {
     case 16: return run_expert<16>(a, status, ws, lay, st);
     case 32: return run_expert<32>(a, status, ws, lay, st);
     case 64: return run_expert<64>(a, status, ws, lay, st);
     case 128: return run_expert<128>(a, status, ws, lay, st);
+    case 208: return run_expert<208>(a, status, ws, lay, st);
     case 224: return run_expert<224>(a, status, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
@@ -1188,7 +1064,7 @@ int check_expert_args(const moe_expert_args *a, bool need_ws) {
       2 * a->I * a->E >= ((int64_t)1 << 31))
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (a->tile_n != 0 && a->tile_n != 16 && a->tile_n != 32 && a->tile_n != 64 && a->tile_n != 128 &&
-      a->tile_n != 224)
+      a->tile_n != 208 && a->tile_n != 224)
     return MOE_ERR_INVALID_ARG;
   if (a->phases & ~15) return MOE_ERR_INVALID_ARG;
   if ((a->phases & MOE_PHASE_H_SCALES) && (!a->hq || !a->hs)) return MOE_ERR_INVALID_ARG;

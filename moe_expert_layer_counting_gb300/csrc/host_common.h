@@ -71,8 +71,8 @@ inline int64_t max_token_tiles(int64_t P, int64_t E, int64_t bn) {
 inline ExpertWs expert_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   const int64_t P = T * k;
   // token-scale chunks: the most (tiles x chunk bytes) over the tile sizes
-  // (16 tokens: most tiles, 512 B chunks; 224 tokens: 1 KB chunks)
-  const int64_t chunks = std::max(max_token_tiles(P, E, 16) * 512, max_token_tiles(P, E, 224) * 1024);
+  // (16 tokens: most tiles, 512 B chunks; 208 tokens: the most 1 KB chunks)
+  const int64_t chunks = std::max(max_token_tiles(P, E, 16) * 512, max_token_tiles(P, E, 208) * 1024);
   ExpertWs w;
   size_t off = 0;
   w.sfb1 = off;    off += round_up((size_t)chunks * (size_t)(H / 128), 256);
@@ -89,9 +89,10 @@ inline ExpertWs expert_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int
 constexpr size_t kStatusBytes = 256;
 
 // Token tile chosen from the mean number of pairs per routed expert: tiles up
-// to 64 tokens run two CTAs per SM; above that a 224-token tile gives each
+// to 64 tokens run two CTAs per SM; above that a large tile gives each
 // tcgen05 instruction more tensor work (the MMA's N follows the tile's valid
-// tokens rounded up to 16).
+// tokens rounded up to 16, or 32 on CTA pairs): 224 here, which
+// resolve_tile_n turns into 208 where the GEMMs run on CTA pairs.
 inline int choose_tile_n(int64_t P, int64_t E) {
   const int64_t ne = E < P ? E : P;
   const int64_t mean = ne > 0 ? ceil_div(P, ne) : 1;
@@ -127,6 +128,15 @@ size_t fused_sync_ints(int64_t T, int E, int k);
 int launch_fused_gemms(const moe_expert_args *a, uint16_t *y, int *sync, int *status, char *ews, cudaStream_t st);
 int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
                  float *wts, int32_t *inv_perm, void *scratch, cudaStream_t st);
+// Large problems (224-token tiles): GEMM1 / GEMM2 on 2-CTA clusters sharing
+// one M = 256 MMA (gemm2sm.cu).  Eligible when both GEMMs' 128-row weight
+// tiles pair up (2I/128 and H/128 even) and the shared memory fits.
+bool pair_eligible(int64_t H, int64_t I, int E);
+// The token tile a call uses: tile_n, or choose_tile_n's when 0; the large
+// tile is 208 tokens on CTA pairs (pair_eligible) and 224 on single CTAs.
+int resolve_tile_n(int tile_n, int64_t P, int64_t E, int64_t H, int64_t I);
+int run_expert_pairs(const moe_expert_args *a, int phases, int *status, uint8_t *hq, uint8_t *sfb1, uint8_t *sfb2,
+                     const float *w_pool, const uint8_t *xq_pool, cudaStream_t st);
 int launch_combine(const uint16_t *y_pairs, const int32_t *idx, int64_t T, int k, int64_t H, uint16_t *y,
                    cudaStream_t st);
 

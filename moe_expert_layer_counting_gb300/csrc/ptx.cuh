@@ -242,17 +242,88 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo,
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling:
 // A = E2M1 (code 5), B = E4M3 (code 0), both K-major, UE8M0 scales,
-// M = 128, N = n; sf_id picks the byte of the 32-bit scale cell.
-__device__ __forceinline__ uint32_t make_idesc_fp4w_fp8a(uint32_t n, uint32_t sf_id) {
+// M = m (128, or 256 for the 2-SM form), N = n; sf_id picks the byte of the
+// 32-bit scale cell.
+__device__ __forceinline__ uint32_t make_idesc_fp4w_fp8a(uint32_t n, uint32_t sf_id, uint32_t m = 128) {
   uint32_t d = 0;
   d |= (sf_id & 3u) << 4;      // B scale-factor byte
   d |= 5u << 7;                // A format: E2M1
   d |= 0u << 10;               // B format: E4M3
   d |= ((n >> 3) & 0x3Fu) << 17;
   d |= 1u << 23;               // scale format UE8M0
-  d |= ((128u >> 4) & 0x1Fu) << 24;
+  d |= ((m >> 4) & 0x1Fu) << 24;
   d |= (sf_id & 3u) << 29;     // A scale-factor byte
   return d;
+}
+
+// ---------------------------------------------------------------- 2-SM (cta_group::2) forms
+// A CTA pair of a 2-CTA cluster shares one MMA: the even CTA (rank 0) issues
+// tcgen05.mma.cta_group::2 with M = 256, each CTA holding 128 rows of A and
+// of D (its own TMEM) and N/2 rows of B (CTA r supplies columns
+// [r*N/2, (r+1)*N/2)); the A scales are each CTA's own rows, the B scales all
+// N columns in each CTA's TMEM; tcgen05.cp.cta_group::2 copies each CTA's
+// shared memory into its own TMEM.  A kernel uses one cta_group throughout.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Barrier over both CTAs of the cluster (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address in the shared memory of cluster CTA `rank` of the variable at
+// shared::cta address `addr` of this CTA.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Both CTAs' warps allocate / free the same TMEM columns together.
+__device__ __forceinline__ void tmem_alloc_2sm(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_2sm() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_2sm(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrives once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
+// when all tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_2sm(uint64_t *bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               ::"r"(smem_u32(bar)), "h"(cta_mask)
+               : "memory");
+}
+__device__ __forceinline__ void tc_cp_2sm_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma_2sm_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                    uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (`bar_cluster`: shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_2sm(void *dst, const CUtensorMap *map, uint32_t bar_cluster, int32_t x,
+                                                int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
 }
 
 // ---------------------------------------------------------------- formats

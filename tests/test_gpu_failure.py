@@ -40,10 +40,12 @@ def _oracle_y(wl, x, logits, l1, l2):
     return O.forward(bits(x), logits.numpy(), w1q, w1s, w2q, w2s, wl.k)["y"]
 
 
-@pytest.mark.parametrize("tile_n", [16, 32])
+@pytest.mark.parametrize("tile_n", [16, 32, 224])
 def test_injected_wait_times_out_then_recovers(monkeypatch, tile_n):
     """tile_n 16: GEMM1 + GEMM2 + combine in one launch (CTAs also wait on
-    one another's arrival counters); 32: separate GEMM launches."""
+    one another's arrival counters); 32: separate GEMM launches; 224: the
+    GEMMs on CTA pairs (the leader's MMA issuer takes the injected wait, the
+    other CTA of each pair must give up through the abort flag)."""
     from helpers import lib
     lib()
     from moe_expert_layer_counting_gb300 import binding as B

@@ -4,7 +4,8 @@ with the oracle.
 moe_forward picks one of three front ends from the problem size: the fused
 small-problem kernel (T <= 64, E <= 256, T*k*H <= 4M), routing + permute + a
 pool cast (P*H <= 16M), or routing + permute + activation cast + pool copy
-(larger), and the token tile from the mean pairs per routed expert.  The
+(larger), and the token tile from the mean pairs per routed expert; 224-token
+tiles run on CTA pairs where the weight tiles pair up.  The
 shapes below are small enough for the float64 oracle, with ragged counts,
 E not a multiple of 32, a single token, k = 1, and a few thousand pairs."""
 import numpy as np
@@ -28,6 +29,10 @@ SHAPES = {
     "wide_H_front": (3, 7168, 128, 9, 2),       # front kernel, 224 column groups
     "large_path": (2048, 1024, 128, 64, 8),     # P*H > 16M: activation cast + pool copy, 224-token tiles
     "one_expert": (40, 256, 128, 1, 1),         # front kernel, E = 1, k = 1: three token tiles of one expert
+    # 224-token tiles on CTA pairs (weight tiles pair up: 2I/128 and H/128 even)
+    "pair_ragged": (700, 512, 256, 6, 2),       # ~233 pairs per expert: one or two tiles, ragged last tile
+    "pair_two_sf_groups": (600, 256, 256, 8, 2),  # ~150 pairs: MMA N = 160, token scales in two 128-row groups
+    "pair_fallback": (300, 384, 128, 4, 2),     # H/128 = 3 odd: the one-CTA 224-token kernel instead
 }
 
 
