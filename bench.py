@@ -83,6 +83,8 @@ def parse():
     ap.add_argument("--only", action="store_true", help="measure only --workload (no per_workload entries)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
+                    help="large CTA-pair problems: 0 library default, 1 separate launches, 2 expert waves (one launch)")
     ap.add_argument("--weights", default="fp4", choices=["fp4", "bfp8"],
                     help="fp4: FP8 x FP4 with UE8M0 per 32 (moe_forward); bfp8: block-FP8 weights (moe_forward_bfp8)")
     ap.add_argument("--no-flush", action="store_true", help="skip the L2 flush (for profiler launch lists)")
@@ -352,7 +354,7 @@ def measure(args, wl, dev, stream, world, rank, headline):
         else:
             B.moe_forward(x, logits, qe.w1q, qe.w1s, qe.w2q, qe.w2s, k, y, ws, topk_idx_out=idx, topk_w_out=wts,
                           counts_out=counts, offsets_out=offsets, perm_out=perm, tile_n=args.tile_n,
-                          phases=phases, stream=st)
+                          phases=phases, schedule=args.schedule, stream=st)
 
     def flush():
         if not args.no_flush:
@@ -367,8 +369,9 @@ def measure(args, wl, dev, stream, world, rank, headline):
     with torch.cuda.graph(graph, stream=stream):
         forward(torch.cuda.current_stream())
     counts_np = counts.cpu().numpy()
-    n_launch_forward = launches_per_forward_bfp8(T, H, E, k) if bfp8 else launches_per_forward(T, H, E, k)
-    fused = (not bfp8) and n_launch_forward == 2            # GEMM1 + GEMM2 + combine in one launch
+    n_launch_forward = (launches_per_forward_bfp8(T, H, E, k) if bfp8 else
+                        launches_per_forward(T, H, I, E, k, args.schedule))
+    fused = (not bfp8) and single_gemm_launch(T, H, I, E, k, args.schedule)   # GEMM1 + GEMM2 + combine, one launch
     loop = lambda fn, n, **kw: timed_loop(stream, fn, n, flush=flush, **kw)  # noqa: E731
 
     if args.launch_list:
@@ -429,7 +432,8 @@ def measure(args, wl, dev, stream, world, rank, headline):
     kname = "bfp8_gemm_kernel" if bfp8 else "expert_gemm_kernel"
     if fused:
         dom, dom_ms = "fused", g_ms
-        what = f"{kname}<16, GEMM1 + GEMM2 + combine> (one launch)"
+        what = (f"{kname}<16, GEMM1 + GEMM2 + combine> (one launch)" if T <= 64 else
+                "expert_gemm_pair_kernel<GEMM1 + GEMM2 + combine> (one launch, CTA pairs, expert waves)")
     else:
         dom = "gemm1" if g1 >= g2 else "gemm2"
         dom_ms = max(g1, g2)
@@ -444,7 +448,8 @@ def measure(args, wl, dev, stream, world, rank, headline):
                    "pairs": T * k, "weights": args.weights + (" (tile-contiguous codes)" if bfp8 else ""),
                    "touched_experts": alg["touched_experts"], "tile_n": args.tile_n or "auto",
                    "l2": "flushed between steps (512 MiB write + 512 MiB read)" if not args.no_flush else "not flushed",
-                   "cuda_graph": True, "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "cuda_graph": True, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "schedule": {0: "default", 1: "separate", 2: "expert waves"}[args.schedule]},
         "layer_roofline_frac": round(layer_time_bound / (mean_ms * 1e-3), 4),
         "layer_rates": layer_rates(alg, mean_ms),
         "gemm_ms": gemm_ms,
@@ -688,7 +693,26 @@ def run_reference(args):
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def launches_per_forward(T, H, E, k):
+def pair_tiles(T, H, I, E, k):
+    """Large problems whose GEMMs run on CTA pairs (208-token tiles; csrc/gemm2sm.cu)."""
+    P = T * k
+    if 1 <= T <= 64 and E <= 256 and P * H <= (4 << 20):
+        return False                           # small-problem front kernel
+    ne = min(E, P)
+    return -(-P // ne) > 64 and (2 * I // 128) % 2 == 0 and (H // 128) % 2 == 0
+
+
+def single_gemm_launch(T, H, I, E, k, schedule=0):
+    """Whether the layer's GEMMs (and the combine) are one launch: small
+    problems with 16-token tiles, or CTA-pair problems under the expert-wave
+    schedule (moe_forward's `schedule` = 2)."""
+    P = T * k
+    if 1 <= T <= 64 and E <= 256 and P * H <= (4 << 20):
+        return -(-P // min(E, P)) <= 16        # 16-token tiles after the front kernel
+    return schedule == 2 and pair_tiles(T, H, I, E, k)
+
+
+def launches_per_forward(T, H, I, E, k, schedule=0):
     """Kernels one moe_forward launches (the dispatch in csrc/api.cu)."""
     P = T * k
     permute = 1 if P <= 2048 else 2            # single-block permute, or count + scatter
@@ -697,9 +721,10 @@ def launches_per_forward(T, H, E, k):
         if -(-P // ne) <= 16:                  # 16-token tiles
             return 2                           # front (route + permute + pool cast), GEMM1 + GEMM2 + combine
         return 4                               # front, GEMM1, GEMM2, combine
-    if P * H <= (16 << 20):
-        return 1 + permute + 1 + 3             # route, permute, pool cast, GEMM1, GEMM2, combine
-    return 1 + 1 + permute + 1 + 3             # quant, route, permute, pool prep, GEMM1, GEMM2, combine
+    cast = 1 if P * H <= (16 << 20) else 2     # pool cast, or activation cast + pool copy
+    if single_gemm_launch(T, H, I, E, k, schedule):
+        return 1 + permute + cast + 1          # route, permute, cast, GEMM1 + GEMM2 + combine
+    return 1 + permute + cast + 3              # route, permute, cast, GEMM1, GEMM2, combine
 
 
 def launches_per_forward_bfp8(T, H, E, k):

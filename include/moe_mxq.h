@@ -265,7 +265,26 @@ typedef struct moe_forward_args {
      * RESET runs before the GEMMs when combined.  Routing, permute and the
      * activation cast are not re-run.  Other bits: MOE_ERR_INVALID_ARG. */
     int32_t phases;
+    /* enum moe_schedule: how large problems whose GEMMs run on CTA pairs
+     * (208-token tiles, see tile_n) schedule GEMM1, GEMM2 and the combine.
+     * Ignored elsewhere.  Other values: MOE_ERR_INVALID_ARG. */
+    int32_t schedule;
 } moe_forward_args;
+
+enum moe_schedule {
+    /* the library's choice: currently MOE_SCHEDULE_SEPARATE (measured faster) */
+    MOE_SCHEDULE_DEFAULT = 0,
+    /* GEMM1, GEMM2 and the combine as three launches */
+    MOE_SCHEDULE_SEPARATE = 1,
+    /* one persistent launch that walks expert waves: GEMM1 items of a wave of
+     * token tiles, then (one wave later) its GEMM2 items, which wait on per-
+     * tile arrival counters, then the combine (MegaMoE (study notes), "Wave",
+     * "Scheduler"; MegaMoE overview, "3. Wave-Based Expert Processing").
+     * Every CTA of the launch must be resident at once (one per SM); if the
+     * GPU is shared so that some cannot be, the waits give up with
+     * MOE_ERR_TIMEOUT instead of hanging. */
+    MOE_SCHEDULE_EXPERT_WAVES = 2
+};
 
 MOE_API size_t moe_workspace_size(int64_t T, int64_t H, int64_t I, int32_t E, int32_t k);
 MOE_API int moe_forward(const moe_forward_args *args, cudaStream_t stream);

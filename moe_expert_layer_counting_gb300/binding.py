@@ -40,6 +40,7 @@ MOE_ERR_DEVICE_INDEX = 7
 
 LAYOUT_CANONICAL, LAYOUT_MMA_L1, LAYOUT_MMA_L2 = 0, 1, 2
 PHASE_TOKEN_SCALES, PHASE_GEMM1, PHASE_GEMM2, PHASE_H_SCALES, PHASE_RESET = 1, 2, 4, 8, 16
+SCHEDULE_DEFAULT, SCHEDULE_SEPARATE, SCHEDULE_EXPERT_WAVES = 0, 1, 2
 ROUTE_SOFTMAX, ROUTE_SIGMOID, ROUTE_RAW, ROUTE_NO_RENORM = 0, 1, 2, 4
 BFP8_LAYOUT_CANONICAL, BFP8_LAYOUT_TILED = 0, 1
 
@@ -74,7 +75,7 @@ class MoeForwardArgs(ctypes.Structure):
                 ("counts_out", _p), ("offsets_out", _p), ("perm_out", _p),
                 ("tile_n", _i32),
                 ("workspace", _p), ("workspace_bytes", _sz),
-                ("route_mode", _i32), ("phases", _i32)]
+                ("route_mode", _i32), ("phases", _i32), ("schedule", _i32)]
 
 
 class MoeBfp8Args(ctypes.Structure):
@@ -241,7 +242,7 @@ def moe_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
 
 def moe_forward(x, logits, w1q, w1s, w2q, w2s, k: int, y, workspace, topk_idx_out=None, topk_w_out=None,
                 counts_out=None, offsets_out=None, perm_out=None, tile_n: int = 0, stream=None, check=True,
-                route_mode: int = ROUTE_SOFTMAX, phases: int = 0) -> int:
+                route_mode: int = ROUTE_SOFTMAX, phases: int = 0, schedule: int = 0) -> int:
     T, H = x.shape
     E = logits.shape[1]
     I = w2q.shape[2] * 2
@@ -249,7 +250,7 @@ def moe_forward(x, logits, w1q, w1s, w2q, w2s, k: int, y, workspace, topk_idx_ou
                        _ptr(x), _ptr(logits), _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s), _ptr(y),
                        _ptr(topk_idx_out), _ptr(topk_w_out), _ptr(counts_out), _ptr(offsets_out),
                        _ptr(perm_out), tile_n, _ptr(workspace), workspace.numel() * workspace.element_size(),
-                       route_mode, phases)
+                       route_mode, phases, schedule)
     rc = lib.moe_forward(ctypes.byref(a), _stream(stream))
     if check:
         _check(rc, "moe_forward")

@@ -111,6 +111,7 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   if (!route_mode_valid(a->route_mode)) return MOE_ERR_INVALID_ARG;
   const int phases = a->phases;
   if (phases & ~(MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2 | MOE_PHASE_RESET)) return MOE_ERR_INVALID_ARG;
+  if (a->schedule < MOE_SCHEDULE_DEFAULT || a->schedule > MOE_SCHEDULE_EXPERT_WAVES) return MOE_ERR_INVALID_ARG;
   if (!a->workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(a->workspace, 256)) return MOE_ERR_MISALIGNED;
   const ForwardWs lay = forward_ws_layout(a->T, a->H, a->I, a->E, a->k);
@@ -148,15 +149,20 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   const int gemms = phases & (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2);
   const int64_t P = a->T * a->k;
   ea.tile_n = resolve_tile_n(a->tile_n, P, a->E, a->H, a->I);
-  const bool fused = a->T > 0 && front_eligible(a->T, a->H, a->E, a->k) &&
-                     fused_eligible(a->T, a->H, a->E, a->k, ea.tile_n);
-  if (fused && gemms != 0 && gemms != (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2)) return MOE_ERR_INVALID_ARG;
+  const bool front = a->T > 0 && front_eligible(a->T, a->H, a->E, a->k);
+  const bool fused = front && fused_eligible(a->T, a->H, a->E, a->k, ea.tile_n);
+  // large problems on CTA pairs, expert-wave schedule: GEMM1 + GEMM2 +
+  // combine in one launch (the default keeps three launches: measured faster)
+  const bool pair_layer = a->T > 0 && !front && ea.tile_n == 208 && a->schedule == MOE_SCHEDULE_EXPERT_WAVES;
+  if ((fused || pair_layer) && gemms != 0 && gemms != (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2))
+    return MOE_ERR_INVALID_ARG;
 
   if ((phases == 0 || (phases & MOE_PHASE_RESET)) && cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (phases != 0) {
     if (gemms == 0 || a->T == 0) return MOE_OK;
     if (fused) return launch_fused_gemms(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
+    if (pair_layer) return launch_pair_layer(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
     ea.phases = gemms;
     return launch_expert_forward(&ea, status, ws + lay.expert, st);
   }
@@ -195,6 +201,16 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
     rc = launch_quant_act(a->x, a->T, a->H, const_cast<uint8_t *>(ea.xq), const_cast<uint8_t *>(ea.xs), st);
     if (rc != MOE_OK) return rc;
     ea.phases = 0;
+  }
+  if (pair_layer) {
+    // the pool rows (prep step, if the cast above did not write them), then
+    // both GEMMs and the combine in one launch
+    if (ea.phases == 0) {
+      ea.phases = MOE_PHASE_TOKEN_SCALES;
+      rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
+      if (rc != MOE_OK) return rc;
+    }
+    return launch_pair_layer(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
   }
   rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
   if (rc != MOE_OK) return rc;

@@ -96,7 +96,7 @@ struct Cfg {
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kKBS * 512;
   static constexpr int kOffEpi = kOffSfb + kStages * kKBS * kTokChunk;   // 4 KB epilogue staging per half
-  // per-item row info, double-buffered by item parity: pair id [2][BN], weight [2][BN]
+  // per-item row info, double-buffered by item parity: y_pairs row [2][BN], weight [2][BN]
   static constexpr int kOffRow = kOffEpi + 4096 * kEpiHalves;
   static constexpr int kOffBar = kOffRow + 16 * BN;
   static constexpr int kNumBars = 2 * kStages + 6;
@@ -106,6 +106,7 @@ struct Cfg {
   static_assert(kStages >= 2, "need at least two stages");
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kTmemAlloc * kCtasPerSm <= 512, "co-resident CTAs share the SM's 512 TMEM columns");
+  static_assert(kThreads / 32 <= 15, "block scan: warp sums in [0, 15), total at 15");
 };
 
 template <int BN>
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
+        if (elect_one()) {
           for (int i = 0; i < nk; ++i) {
             const uint32_t sf_col = tmem_base + (uint32_t)(C::kAccBufs * BN + C::kSfSlot * (stage * C::kKBS + i));
             const uint32_t sfa = smem_u32(smem + C::kOffSfa + (stage * C::kKBS + i) * 512);
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&tmem_full[acc]);
+      if (elect_one()) tc_commit(&tmem_full[acc]);
       __syncwarp();
       if (++acc == C::kAccBufs) { acc = 0; acc_phase ^= 1; }
     }
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
       float *row_w = row_w_buf + rb * BN;
       if (et < ti.valid) {
         if (it.l1) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
-        else row_pair[et] = __ldg(args.perm + ti.s0 + et);
+        else row_pair[et] = pair_row(__ldg(args.perm + ti.s0 + et), args.k, args.T);
       }
       // the epilogue warps agree on the outcome of the bounded wait before any
       // of them enters another named barrier
@@ -486,8 +487,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
           epilogue_gemm1_chunk(v, c0, q, lane, ti, row_w, ebuf_f, bar_half, args.I, C::kTokChunk, args.hq,
                                args.sfb2, args.hs_out);
         else
-          epilogue_gemm2_chunk(v, c0, q, lane, ti, row_pair, ebuf_h, bar_half, args.k, args.T, args.H,
-                               args.y_pairs);
+          epilogue_gemm2_chunk(v, c0, q, lane, ti, row_pair, ebuf_h, bar_half, args.H, args.y_pairs);
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
@@ -529,41 +529,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, Cfg<BN>::kCtasPerSm)
     // (token, 8-value chunk) items in FP32, in slot order, and casts once
     if (threadIdx.x == 0) scan_ws[0] = wait_counter(args.sync, n2, status, kWaitLimit, total_work) ? 1 : 0;
     __syncthreads();
-    if (scan_ws[0]) {
-      const int H8 = args.H / 8;
-      const int items = args.T * H8;
-      const uint4 *yp = reinterpret_cast<const uint4 *>(args.y_pairs);
-      for (int i = (int)blockIdx.x * C::kThreads + (int)threadIdx.x; i < items; i += (int)gridDim.x * C::kThreads) {
-        const int t = i / H8;
-        float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j0 = 0; j0 < args.k; j0 += 8) {
-          bool use[8];
-          uint4 v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) use[u] = j0 + u < args.k && __ldg(args.topk_idx + t * args.k + j0 + u) >= 0;
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (use[u]) v[u] = __ldcg(yp + (size_t)(j0 + u) * items + i);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (!use[u]) continue;
-            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
-              acc8[2 * q2] += bf16_bits_to_float(wv[q2] & 0xFFFFu);
-              acc8[2 * q2 + 1] += bf16_bits_to_float(wv[q2] >> 16);
-            }
-          }
-        }
-        uint32_t o[4];
-#pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc8[2 * q2], acc8[2 * q2 + 1]);
-          o[q2] = *reinterpret_cast<const uint32_t *>(&b2);
-        }
-        args.y[i] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
+    if (scan_ws[0])
+      combine_share(args.y_pairs, args.topk_idx, args.T, args.k, args.H, args.y,
+                    (int)blockIdx.x * C::kThreads + (int)threadIdx.x, (int)gridDim.x * C::kThreads);
   }
 }
 

@@ -15,9 +15,10 @@
 //   * one thread issues for two SMs: four MMAs and three scale copies per
 //     128-wide K block keep both tensor cores ~97 % busy at N = 224 (measured
 //     issue rate), and token rows cross L2 -> SM once per pair, not per SM.
-// Roles per CTA (320 threads): warp 0 TMA producer (both CTAs), warp 1 TMEM
-// allocation (both) and the MMA issuer (rank 0 only), warps 2-9 epilogue
-// (both; two halves of four warps, one TMEM lane quadrant per warp).
+// Roles per CTA (640 threads): warps 0-1 TMA producers of the two issue
+// streams (both CTAs), warps 2-3 their MMA issuers (rank 0 only; warp 2 also
+// allocates TMEM in both CTAs), warps 4-19 epilogue (both CTAs; four column
+// groups of four warps, one TMEM lane quadrant per warp).
 // Synchronisation of the pair:
 //   * every load of either CTA counts on the leader's `full` barrier (TMA
 //     .cta_group::2 form); the leader's producer arms it for both CTAs' bytes;
@@ -47,7 +48,8 @@ struct Pair {
   static constexpr int kStreams = 2;                      // independent issue streams of a pair
   static constexpr int kStagesPerStream = 3;
   static constexpr int kStages = kStreams * kStagesPerStream;
-  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiWarps = 16;                    // four groups of four (one TMEM lane quadrant each)
+  static constexpr int kEpiGroups = kEpiWarps / 4;
   static constexpr int kFirstEpiWarp = 2 * kStreams;      // warps 0-1 producers, 2-3 MMA issuers
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
   static constexpr int kATile = kBM * kBK;                // unpacked FP4 weight tile (8-bit containers)
@@ -64,38 +66,139 @@ struct Pair {
   static constexpr int kOffSfa = kOffB + kStages * kBTile;
   static constexpr int kOffSfb = kOffSfa + kStages * 512;
   static constexpr int kOffEpi = kOffSfb + kStages * kTokChunk;
-  static constexpr int kOffRow = kOffEpi + 4096 * 2;      // pair id [2][BN], weight [2][BN]
+  static constexpr int kOffRow = kOffEpi + 4096 * kEpiGroups;   // y_pairs row [2][BN], weight [2][BN]
   static constexpr int kOffBar = kOffRow + 16 * kBN;
   // full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], mma_done[2], never
   static constexpr int kNumBars = 2 * kStages + 3 * kStreams + 1;
   static constexpr int kOffTmemPtr = (kOffBar + 8 * kNumBars + 63) & ~63;
-  static constexpr int kOffScan = kOffTmemPtr + 64;
-  static constexpr int kOffExp = kOffScan + 64;
+  static constexpr int kOffScan = kOffTmemPtr + 64;      // block scan: warp sums [0, 32), total [32]
+  static constexpr int kOffExp = kOffScan + 256;
   static_assert(kTmemCols <= 512, "TMEM budget");
   static_assert(kBTile % 1024 == 0 && kATile % 1024 == 0, "stage buffers stay 1024-byte aligned");
   static_assert(kHalf % 8 == 0, "token half-tiles are whole 8-row swizzle atoms");
+  static_assert(kThreads / 32 <= 32, "block scan: one warp sum per warp in 32 slots");
 };
 
 size_t pair_smem_bytes(int E) { return 1024 + Pair::kOffExp + (size_t)3 * (E + 1) * 4; }
 
+// Both GEMMs' tensor maps (PHASE 1 and 2 use the set of their GEMM).
+struct PairMaps {
+  CUtensorMap w[2];      // weight codes (FP4, unpacked by TMA), one per GEMM
+  CUtensorMap b[2];      // token rows: pool rows (GEMM1), h rows (GEMM2)
+  CUtensorMap wsf[2];    // weight scale chunks, viewed as [rows][256] bytes
+  CUtensorMap bsf[2];    // token scale chunks, viewed as [rows][256] bytes
+};
+
 struct PairArgs {
   int E, k, T, H, I;
-  int KB, MT;                       // K blocks, 128-row weight tiles per expert (even)
+  int KB[2], MT[2];                 // per GEMM: K blocks, 128-row weight tiles per expert (even)
   int inject_wait;                  // debug: the MMA issuers first wait on a barrier nothing completes
-  const uint8_t *w_codes;           // L2 prefetch ahead of the weight loads
+  const uint8_t *w_codes[2];        // L2 prefetch ahead of the weight loads
   const int32_t *counts, *offsets, *perm;
   const float *w_pool;              // GEMM1 epilogue: top-k weight of each pool row
   uint8_t *hq, *sfb2, *hs_out;      // GEMM1 outputs
   uint16_t *y_pairs;                // GEMM2 output
   int *status;
+  // PHASE 3: arrival counters ([0] GEMM2 CTA-items done, [1 + g] GEMM1
+  // CTA-items of token tile g done; zeroed before the launch) and the combine
+  int *sync;
+  const int32_t *topk_idx;
+  uint4 *y;
 };
+
+// Expert waves of the single launch: kWaveTiles token tiles (expert-major
+// order) per wave, the last wave possibly shorter.  Each wave's GEMM1 items
+// (tile-major, weight-row pairs fastest) come one wave ahead of its GEMM2
+// items:  [L1 w0] [L1 w1] [L2 w0] [L1 w2] [L2 w1] ... [L2 last].  A GEMM2 item
+// depends only on the GEMM1 items of its own tile, which sit at least a whole
+// wave of GEMM1 items (kWaveTiles * MT1/2 = 384 here, ~2.5x the items in
+// flight on 152 SMs) earlier in the list, so it seldom waits, and every
+// dependency points to a smaller index (the lowest unfinished item never
+// waits).  h of about two waves is live in L2 at a time.
+constexpr int kWaveTiles = 24;
+
+struct PairItem {
+  int gemm;                         // 0: GEMM1, 1: GEMM2
+  TileInfo ti;                      // ti.mt = weight-row pair
+};
+
+// Token tile g -> expert, first pool row and valid rows (tile_off: first
+// tile of each expert).
+__device__ __forceinline__ void tile_rows(int g, int E, int bn, const int *tile_off, const int *cnt_sm,
+                                          const int *off_sm, TileInfo &ti) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_off[mid] <= g) lo = mid; else hi = mid;
+  }
+  ti.e = lo;
+  ti.g = g;
+  const int nt = g - tile_off[lo];
+  ti.s0 = off_sm[lo] + nt * bn;
+  const int rem = cnt_sm[lo] - nt * bn;
+  ti.valid = rem < bn ? rem : bn;
+}
+
+template <int PHASE>
+__device__ __forceinline__ PairItem decode_pair_item(int w, const PairArgs &args, int NT, const int *tile_off,
+                                                     const int *cnt_sm, const int *off_sm) {
+  PairItem it;
+  int g;
+  if (PHASE != 3) {
+    const int MT2 = args.MT[PHASE - 1] >> 1;
+    it.gemm = PHASE - 1;
+    g = w / MT2;
+    it.ti.mt = w - g * MT2;
+  } else {
+    const int m1 = args.MT[0] >> 1, m2 = args.MT[1] >> 1;
+    const int nw = (NT + kWaveTiles - 1) / kWaveTiles;          // waves
+    const int nlast = NT - (nw - 1) * kWaveTiles;               // tiles of the last wave
+    const int n0 = nw > 1 ? kWaveTiles : nlast;
+    int r = w;
+    // block 0: GEMM1 of wave 0
+    if (r < n0 * m1) {
+      it.gemm = 0; g = r / m1; it.ti.mt = r % m1;
+    } else {
+      r -= n0 * m1;
+      // blocks 1 .. nw-2 (full size): GEMM1 of wave b, then GEMM2 of wave b-1
+      const int per_block = kWaveTiles * (m1 + m2);
+      const int full_blocks = nw > 2 ? nw - 2 : 0;
+      if (r < full_blocks * per_block) {
+        const int b = 1 + r / per_block;
+        r -= (b - 1) * per_block;
+        if (r < kWaveTiles * m1) {
+          it.gemm = 0; g = b * kWaveTiles + r / m1; it.ti.mt = r % m1;
+        } else {
+          r -= kWaveTiles * m1;
+          it.gemm = 1; g = (b - 1) * kWaveTiles + r / m2; it.ti.mt = r % m2;
+        }
+      } else {
+        r -= full_blocks * per_block;
+        const int b = nw - 1;                                     // the last wave
+        if (nw >= 2 && r < nlast * m1) {                          // block nw-1: GEMM1 of the last wave ...
+          it.gemm = 0; g = b * kWaveTiles + r / m1; it.ti.mt = r % m1;
+        } else {
+          if (nw >= 2) r -= nlast * m1;
+          if (nw >= 2 && r < kWaveTiles * m2) {                   // ... then GEMM2 of the wave before
+            it.gemm = 1; g = (b - 1) * kWaveTiles + r / m2; it.ti.mt = r % m2;
+          } else {
+            if (nw >= 2) r -= kWaveTiles * m2;
+            it.gemm = 1; g = b * kWaveTiles + r / m2; it.ti.mt = r % m2;   // block nw: GEMM2 of the last wave
+          }
+        }
+      }
+    }
+  }
+  tile_rows(g, args.E, Pair::kBN, tile_off, cnt_sm, off_sm, it.ti);
+  return it;
+}
 
 template <int PHASE>
 __global__ void __launch_bounds__(Pair::kThreads, 1)
-    expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
-                            const __grid_constant__ CUtensorMap tmap_wsf,
-                            const __grid_constant__ CUtensorMap tmap_bsf, const PairArgs args) {
-  // PHASE 1: GEMM1 + SwiGLU epilogue; 2: GEMM2.
+    expert_gemm_pair_kernel(const __grid_constant__ PairMaps maps, const PairArgs args) {
+  // PHASE 1: GEMM1 + SwiGLU epilogue; 2: GEMM2; 3: expert waves of GEMM1
+  // then GEMM2 items in one launch, GEMM2 items waiting on their token
+  // tile's arrival counter, then the combine.
   // A cluster's j-th work item belongs to stream j % 2: producer warp s loads
   // it into stages [3s, 3s+3), MMA warp 2+s (leader) accumulates it into
   // accumulator s; the epilogue warps drain the accumulators in item order.
@@ -134,13 +237,16 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   int n_items = 0;
 #endif
 
-  if (PHASE == 2) pdl_launch_dependents();
+  if (PHASE != 1) pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_w);
-      tma_prefetch_desc(&tmap_b);
-      tma_prefetch_desc(&tmap_wsf);
-      tma_prefetch_desc(&tmap_bsf);
+      for (int gm = 0; gm < 2; ++gm) {
+        if (PHASE != 3 && gm != PHASE - 1) continue;
+        tma_prefetch_desc(&maps.w[gm]);
+        tma_prefetch_desc(&maps.b[gm]);
+        tma_prefetch_desc(&maps.wsf[gm]);
+        tma_prefetch_desc(&maps.bsf[gm]);
+      }
     }
   } else if (warp == 2) {
     if (lane == 0) {
@@ -168,11 +274,12 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   if (PHASE == 1) pdl_launch_dependents();
   load_expert_table(args.counts, args.offsets, args.E, cnt_sm, off_sm);
   __syncthreads();
-  block_tile_map<C::kThreads>(cnt_sm, args.E, C::kBN, tile_off, scan_ws, scan_ws + 15);
+  block_tile_map<C::kThreads>(cnt_sm, args.E, C::kBN, tile_off, scan_ws, scan_ws + 32);
   __syncthreads();
   const uint32_t tmem_base = *tmem_ptr;
-  const int MT2 = args.MT >> 1;                    // weight-row pairs per expert
-  const int total_work = tile_off[args.E] * MT2;
+  const int NT = tile_off[args.E];                 // token tiles
+  const int total_work = PHASE == 3 ? NT * ((args.MT[0] + args.MT[1]) >> 1) : NT * (args.MT[PHASE - 1] >> 1);
+  const int n2_cta_items = 2 * NT * (args.MT[1] >> 1);   // PHASE 3: GEMM2 items x 2 CTAs
 
   if (warp < C::kStreams) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
@@ -180,13 +287,73 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;
-    for (int w = cluster + st * nclusters; w < total_work; w += C::kStreams * nclusters) {
-      const TileInfo ti = decode_work<C::kBN>(w, MT2, args.E, tile_off, cnt_sm, off_sm);
+    bool ok = true;
+    for (int w = cluster + st * nclusters; w < total_work && ok; w += C::kStreams * nclusters) {
+      const PairItem it = decode_pair_item<PHASE>(w, args, NT, tile_off, cnt_sm, off_sm);
+      const TileInfo &ti = it.ti;
+      const int gm = it.gemm;
+      const int KB = args.KB[gm];
       const int n_mma = min(C::kBN, (ti.valid + 31) & ~31);
       const int mt = 2 * ti.mt + (int)rank;                       // this CTA's 128-row weight tile
-      const int wtile = (ti.e * args.MT + mt) * args.KB;
-      bool ok = true;
-      for (int kb = 0; kb < args.KB; ++kb) {
+      const int wtile = (ti.e * args.MT[gm] + mt) * KB;
+      const CUtensorMap *tw = &maps.w[gm], *tb = &maps.b[gm], *twsf = &maps.wsf[gm], *tbsf = &maps.bsf[gm];
+      // one stage = the weight part (codes + scales, static data) and the
+      // token part (pool rows or h + token scales); the leader's barrier
+      // counts both CTAs' bytes of both parts
+      auto issue_weights = [&](int gs, int kb) {
+        const uint32_t bar = mapa_shared(smem_u32(&full[gs]), 0);
+        if (rank == 0) mbar_arrive_expect_tx(&full[gs], C::kStageTx);
+        tma_load_2d_2sm(smem + C::kOffA + gs * C::kATile, tw, bar, 0, (wtile + kb) * kBM);
+        tma_load_2d_2sm(smem + C::kOffSfa + gs * 512, twsf, bar, 0, (wtile + kb) * 2);
+        if (kb + kPrefetchAhead < KB)
+          prefetch_l2_bulk(args.w_codes[gm] + ((size_t)wtile + kb + kPrefetchAhead) * kWTileBytes, kWTileBytes);
+      };
+      auto issue_tokens = [&](int gs, int kb) {
+        const uint32_t bar = mapa_shared(smem_u32(&full[gs]), 0);
+        tma_load_2d_2sm(smem + C::kOffB + gs * C::kBTile, tb, bar, kb * kBK, ti.s0 + (int)rank * (n_mma >> 1));
+        tma_load_2d_2sm(smem + C::kOffSfb + gs * C::kTokChunk, tbsf, bar, 0, (ti.g * KB + kb) * 4);
+      };
+      int kb = 0;
+      if (PHASE == 3 && gm == 1) {
+        // GEMM2 item of the single launch: the weight part of the first
+        // stages, then the wait for the tile's h (every GEMM1 CTA-item of the
+        // tile published), then their token parts -- issued even after a
+        // failed wait, so that every armed barrier completes
+        const int npre = min(KB, C::kStagesPerStream);
+        int armed = 0;
+        const int st0 = stage;
+        const uint32_t ph0 = phase;
+        for (; armed < npre; ++armed) {
+          const int gs = st * C::kStagesPerStream + stage;
+          if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(0, mbar_wait(&empty[gs], phase ^ 1, status, kWaitLimit,
+                                                                   kWaitProducerEmpty, armed))))
+            break;
+          if (lane == 0) issue_weights(gs, armed);
+          __syncwarp();
+          if (++stage == C::kStagesPerStream) { stage = 0; phase ^= 1; }
+        }
+        bool dep_ok = true;
+        if (lane == 0) {
+          dep_ok = wait_counter(args.sync + 1 + ti.g, args.MT[0], status, kWaitLimit, w);
+          fence_proxy_async_global();
+        }
+        dep_ok = __shfl_sync(0xffffffffu, dep_ok ? 1 : 0, 0) != 0;
+        for (int a = 0; a < armed; ++a) {
+          const int sa = (st0 + a) % C::kStagesPerStream;
+          const uint32_t pa = ph0 ^ (uint32_t)((st0 + a) / C::kStagesPerStream);
+          const int gs = st * C::kStagesPerStream + sa;
+          if (lane == 0) issue_tokens(gs, a);
+          issued_mask |= 1u << gs;
+          issued_phase = (issued_phase & ~(1u << gs)) | (pa << gs);
+        }
+        __syncwarp();
+        if (armed < npre || !dep_ok) {
+          ok = false;
+          break;
+        }
+        kb = npre;
+      }
+      for (; kb < KB; ++kb) {
         const int gs = st * C::kStagesPerStream + stage;
         if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(0, mbar_wait(&empty[gs], phase ^ 1, status, kWaitLimit,
                                                                  kWaitProducerEmpty, kb)))) {
@@ -194,22 +361,14 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
           break;
         }
         if (lane == 0) {
-          if (rank == 0) mbar_arrive_expect_tx(&full[gs], C::kStageTx);
-          const uint32_t bar = mapa_shared(smem_u32(&full[gs]), 0);
-          tma_load_2d_2sm(smem + C::kOffA + gs * C::kATile, &tmap_w, bar, 0, (wtile + kb) * kBM);
-          tma_load_2d_2sm(smem + C::kOffB + gs * C::kBTile, &tmap_b, bar, kb * kBK,
-                          ti.s0 + (int)rank * (n_mma >> 1));
-          tma_load_2d_2sm(smem + C::kOffSfa + gs * 512, &tmap_wsf, bar, 0, (wtile + kb) * 2);
-          tma_load_2d_2sm(smem + C::kOffSfb + gs * C::kTokChunk, &tmap_bsf, bar, 0, (ti.g * args.KB + kb) * 4);
-          if (kb + kPrefetchAhead < args.KB)
-            prefetch_l2_bulk(args.w_codes + ((size_t)wtile + kb + kPrefetchAhead) * kWTileBytes, kWTileBytes);
+          issue_weights(gs, kb);
+          issue_tokens(gs, kb);
         }
         __syncwarp();
         issued_mask |= 1u << gs;
         issued_phase = (issued_phase & ~(1u << gs)) | (phase << gs);
         if (++stage == C::kStagesPerStream) { stage = 0; phase ^= 1; }
       }
-      if (!ok) break;
     }
     // the leader never leaves with copies in flight (its full barriers count
     // both CTAs' bytes; the other CTA's copies are covered by the final
@@ -236,8 +395,9 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
       bool ok = true;
       const uint32_t d_tmem = tmem_base + (uint32_t)(st * C::kBN);
       for (int w = cluster + st * nclusters; w < total_work && ok; w += C::kStreams * nclusters) {
-        const TileInfo ti = decode_work<C::kBN>(w, MT2, args.E, tile_off, cnt_sm, off_sm);
-        const uint32_t n_mma = (uint32_t)min(C::kBN, (ti.valid + 31) & ~31);
+        const PairItem it = decode_pair_item<PHASE>(w, args, NT, tile_off, cnt_sm, off_sm);
+        const int KB = args.KB[it.gemm];
+        const uint32_t n_mma = (uint32_t)min(C::kBN, (it.ti.valid + 31) & ~31);
         if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(2, mbar_wait(&tmem_empty[st], acc_phase ^ 1, status, kWaitLimit,
                                                                  kWaitMmaTmemEmpty, w))))
           break;
@@ -245,18 +405,19 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
             !__all_sync(0xffffffffu, mbar_wait(never, 0, status, kInjectedWaitLimit, kWaitInjected, w)))
           break;
         tc_fence_after();
-        for (int kb = 0; kb < args.KB; ++kb) {
+        for (int kb = 0; kb < KB; ++kb) {
           const int gs = st * C::kStagesPerStream + stage;
           if (!__all_sync(0xffffffffu,
                           MXQ_TIMED_WAIT(1, mbar_wait(&full[gs], phase, status, kWaitLimit, kWaitMmaFull, kb)))) {
             ok = false;
             break;
           }
-          tc_fence_after();
+          // (no tcgen05 fence: the stage's bytes are published by the
+          // mbarrier's transaction count, which the wait observed)
 #ifdef MOE_MXQ_WAIT_STATS
           const long long t_issue = clock64();
 #endif
-          if (lane == 0) {
+          if (elect_one()) {
             const uint32_t sf_col = tmem_base + (uint32_t)(C::kTmemAcc + C::kSfSlot * gs);
             const uint32_t sfa = smem_u32(smem + C::kOffSfa + gs * 512);
             const uint32_t sfb = smem_u32(smem + C::kOffSfb + gs * C::kTokChunk);
@@ -281,7 +442,7 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
           if (++stage == C::kStagesPerStream) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        if (lane == 0) tc_commit_2sm(&tmem_full[st], 3);
+        if (elect_one()) tc_commit_2sm(&tmem_full[st], 3);
         __syncwarp();
         acc_phase ^= 1;
       }
@@ -294,23 +455,24 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     const int ew = warp - C::kFirstEpiWarp;
-    const int eh = ew >> 2;
+    const int eg = ew >> 2;                      // column group: chunks eg, eg + 4, ...
     const int et = threadIdx.x - 32 * C::kFirstEpiWarp;
-    const uint32_t bar_half = 2 + eh;
-    float *ebuf_f = reinterpret_cast<float *>(smem + C::kOffEpi + 4096 * eh);
-    uint16_t *ebuf_h = reinterpret_cast<uint16_t *>(smem + C::kOffEpi + 4096 * eh);
+    const uint32_t bar_group = 2 + eg;
+    float *ebuf_f = reinterpret_cast<float *>(smem + C::kOffEpi + 4096 * eg);
+    uint16_t *ebuf_h = reinterpret_cast<uint16_t *>(smem + C::kOffEpi + 4096 * eg);
     int rb = 0;
     int j = 0;                                   // this cluster's item count
     for (int w = cluster; w < total_work; w += nclusters, ++j) {
       const int acc = j & 1;
       const uint32_t acc_phase = (uint32_t)(j >> 1) & 1u;
-      TileInfo ti = decode_work<C::kBN>(w, MT2, args.E, tile_off, cnt_sm, off_sm);
+      const PairItem it = decode_pair_item<PHASE>(w, args, NT, tile_off, cnt_sm, off_sm);
+      TileInfo ti = it.ti;
       ti.mt = 2 * ti.mt + (int)rank;                              // this CTA's weight tile
       int32_t *row_pair = row_pair_buf + rb * C::kBN;
       float *row_w = row_w_buf + rb * C::kBN;
       if (et < ti.valid) {
-        if (PHASE == 1) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
-        else row_pair[et] = __ldg(args.perm + ti.s0 + et);
+        if (it.gemm == 0) row_w[et] = __ldg(args.w_pool + ti.s0 + et);
+        else row_pair[et] = pair_row(__ldg(args.perm + ti.s0 + et), args.k, args.T);
       }
       const bool got = __all_sync(0xffffffffu, MXQ_TIMED_WAIT(3, mbar_wait(&tmem_full[acc], acc_phase, status,
                                                                           kWaitLimit, kWaitEpiTmemFull, w)));
@@ -324,16 +486,24 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
       if (!all_got) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * C::kBN);
-      for (int c0 = kChunk * eh; c0 < ti.valid; c0 += kChunk * 2) {
-        uint32_t v[16];
-        tmem_ld_32x32b_x16(t_row + (uint32_t)c0, v);
+      // TMEM loads one chunk ahead: the next chunk's load is in flight while
+      // this one is processed
+      uint32_t v[16];
+      int c0 = kChunk * eg;
+      if (c0 < ti.valid) tmem_ld_32x32b_x16(t_row + (uint32_t)c0, v);
+      while (c0 < ti.valid) {
         tmem_ld_wait();
-        if (PHASE == 1)
-          epilogue_gemm1_chunk(v, c0, q, lane, ti, row_w, ebuf_f, bar_half, args.I, C::kTokChunk, args.hq,
+        uint32_t cur[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cur[i] = v[i];
+        const int cn = c0 + kChunk * C::kEpiGroups;
+        if (cn < ti.valid) tmem_ld_32x32b_x16(t_row + (uint32_t)cn, v);
+        if (it.gemm == 0)
+          epilogue_gemm1_chunk(cur, c0, q, lane, ti, row_w, ebuf_f, bar_group, args.I, C::kTokChunk, args.hq,
                                args.sfb2, args.hs_out);
         else
-          epilogue_gemm2_chunk(v, c0, q, lane, ti, row_pair, ebuf_h, bar_half, args.k, args.T, args.H,
-                               args.y_pairs);
+          epilogue_gemm2_chunk(cur, c0, q, lane, ti, row_pair, ebuf_h, bar_group, args.H, args.y_pairs);
+        c0 = cn;
       }
       tc_fence_before();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
@@ -341,6 +511,17 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
       if (lane == 0 && ew == 0) wait_acc[5] += clock64() - t_epi;
 #endif
       rb ^= 1;
+      if (PHASE == 3) {
+        // publish the CTA-item: GEMM1 -> its h rows and scale bytes (read by
+        // other CTAs' TMA: proxy fence, then release), GEMM2 -> its y_pairs
+        // rows (read by the combine)
+        if (it.gemm == 0) fence_proxy_async_global();
+        named_bar_sync(1, 32 * C::kEpiWarps);
+        if (et == 0) {
+          __threadfence();
+          atomicAdd(it.gemm == 0 ? args.sync + 1 + ti.g : args.sync, 1);
+        }
+      }
     }
   }
 #ifdef MOE_MXQ_WAIT_STATS
@@ -363,6 +544,14 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc_2sm(tmem_base, 512);
+  }
+  if (PHASE == 3) {
+    // the combine, once every GEMM2 CTA-item of the launch has published its rows
+    if (threadIdx.x == 0) scan_ws[0] = wait_counter(args.sync, n2_cta_items, status, kWaitLimit, total_work) ? 1 : 0;
+    __syncthreads();
+    if (scan_ws[0])
+      combine_share(args.y_pairs, args.topk_idx, args.T, args.k, args.H, args.y,
+                    (int)blockIdx.x * C::kThreads + (int)threadIdx.x, (int)gridDim.x * C::kThreads);
   }
 }
 
@@ -413,57 +602,93 @@ int resolve_tile_n(int tile_n, int64_t P, int64_t E, int64_t H, int64_t I) {
   return bn;
 }
 
-// GEMM1 (phase bit MOE_PHASE_GEMM1) and / or GEMM2 (MOE_PHASE_GEMM2) of a
-// 208-token-tile problem on CTA pairs; GEMM1 reads the pool rows and token-
-// scale chunks (sfb1) that the prep / cast kernels wrote and writes h (hq)
-// and GEMM2's token-scale chunks (sfb2), which GEMM2 reads.
-int run_expert_pairs(const moe_expert_args *a, int phases, int *status, uint8_t *hq, uint8_t *sfb1, uint8_t *sfb2,
-                     const float *w_pool, const uint8_t *xq_pool, cudaStream_t st) {
+// Tensor maps of one GEMM (gm 0: GEMM1 on the pool rows, 1: GEMM2 on h).
+bool encode_pair_maps(const moe_expert_args *a, int gm, const uint8_t *tokens, const uint8_t *tok_chunks,
+                      PairMaps &m) {
   const int64_t P = a->T * a->k;
   const int E = a->E;
-  const size_t sm = pair_smem_bytes(E);
-  const int grid = num_sms() & ~1;
+  const int KB = gm == 0 ? (int)(a->H / 128) : (int)(a->I / 128);
+  const int MT = gm == 0 ? (int)(2 * a->I / 128) : (int)(a->H / 128);
+  const uint64_t K = gm == 0 ? (uint64_t)a->H : (uint64_t)a->I;
+  const uint64_t wrows = (uint64_t)E * MT * KB * 128;
   const int64_t max_tiles = max_token_tiles(P, E, Pair::kBN);
+  const uint8_t *wq = gm == 0 ? a->w1q : a->w2q;
+  const uint8_t *ws = gm == 0 ? a->w1s : a->w2s;
+  bool ok = encode_tmap_2d(&m.w[gm], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)wq, 128, wrows, 64, 128, kBM,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&m.b[gm], CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)tokens, K, (uint64_t)P, K, 128,
+                            Pair::kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&m.wsf[gm], CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)ws, 256, (uint64_t)E * MT * KB * 2,
+                            256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  ok = ok && encode_tmap_2d(&m.bsf[gm], CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)tok_chunks, 256,
+                            (uint64_t)max_tiles * KB * 4, 256, 256, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
+  return ok;
+}
+
+PairArgs pair_args(const moe_expert_args *a, int *status, uint8_t *hq, uint8_t *sfb2, const float *w_pool) {
   PairArgs g{};
-  g.E = E; g.k = a->k; g.T = (int)a->T; g.H = (int)a->H; g.I = (int)a->I;
+  g.E = a->E; g.k = a->k; g.T = (int)a->T; g.H = (int)a->H; g.I = (int)a->I;
+  g.KB[0] = (int)(a->H / 128); g.MT[0] = (int)(2 * a->I / 128);
+  g.KB[1] = (int)(a->I / 128); g.MT[1] = (int)(a->H / 128);
+  g.w_codes[0] = a->w1q; g.w_codes[1] = a->w2q;
   g.counts = a->counts; g.offsets = a->offsets; g.perm = a->perm; g.w_pool = w_pool;
   g.hq = hq; g.sfb2 = sfb2; g.hs_out = a->hs; g.y_pairs = a->y_pairs; g.status = status;
   if (const char *env = getenv("MOE_MXQ_DEBUG_INJECT_WAIT")) g.inject_wait = atoi(env);
+  return g;
+}
+
+// GEMM1 (phase bit MOE_PHASE_GEMM1) and / or GEMM2 (MOE_PHASE_GEMM2) of a
+// 208-token-tile problem on CTA pairs, as separate launches; GEMM1 reads the
+// pool rows and token-scale chunks (sfb1) that the prep / cast kernels wrote
+// and writes h (hq) and GEMM2's token-scale chunks (sfb2), which GEMM2 reads.
+int run_expert_pairs(const moe_expert_args *a, int phases, int *status, uint8_t *hq, uint8_t *sfb1, uint8_t *sfb2,
+                     const float *w_pool, const uint8_t *xq_pool, cudaStream_t st) {
+  const size_t sm = pair_smem_bytes(a->E);
+  const int grid = num_sms() & ~1;
+  PairArgs g = pair_args(a, status, hq, sfb2, w_pool);
   if (phases & MOE_PHASE_GEMM1) {
-    const int KB = (int)(a->H / 128), MT = (int)(2 * a->I / 128);
-    const uint64_t wrows = (uint64_t)E * MT * KB * 128;
-    CUtensorMap tw, tb, twsf, tbsf;
-    bool ok = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w1q, 128, wrows, 64, 128, kBM,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)xq_pool, (uint64_t)a->H, (uint64_t)P,
-                              (uint64_t)a->H, 128, Pair::kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && encode_tmap_2d(&twsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a->w1s, 256, (uint64_t)E * MT * KB * 2,
-                              256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok = ok && encode_tmap_2d(&tbsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)sfb1, 256, (uint64_t)max_tiles * KB * 4,
-                              256, 256, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok) return MOE_ERR_CUDA;
-    g.KB = KB; g.MT = MT; g.w_codes = a->w1q;
+    PairMaps m{};
+    if (!encode_pair_maps(a, 0, xq_pool, sfb1, m)) return MOE_ERR_CUDA;
     if (!set_pair_attrs(expert_gemm_pair_kernel<1>, sm)) return MOE_ERR_CUDA;
-    if (launch_pair(expert_gemm_pair_kernel<1>, grid, sm, st, tw, tb, twsf, tbsf, g) != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_pair(expert_gemm_pair_kernel<1>, grid, sm, st, m, g) != MOE_OK) return MOE_ERR_CUDA;
   }
   if (phases & MOE_PHASE_GEMM2) {
-    const int KB = (int)(a->I / 128), MT = (int)(a->H / 128);
-    const uint64_t wrows = (uint64_t)E * MT * KB * 128;
-    CUtensorMap tw, th, twsf, thsf;
-    bool ok = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, (void *)a->w2q, 128, wrows, 64, 128, kBM,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && encode_tmap_2d(&th, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)hq, (uint64_t)a->I, (uint64_t)P,
-                              (uint64_t)a->I, 128, Pair::kHalf, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && encode_tmap_2d(&twsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a->w2s, 256, (uint64_t)E * MT * KB * 2,
-                              256, 256, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok = ok && encode_tmap_2d(&thsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)sfb2, 256, (uint64_t)max_tiles * KB * 4,
-                              256, 256, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (!ok) return MOE_ERR_CUDA;
-    g.KB = KB; g.MT = MT; g.w_codes = a->w2q; g.hs_out = nullptr;
+    PairMaps m{};
+    if (!encode_pair_maps(a, 1, hq, sfb2, m)) return MOE_ERR_CUDA;
+    g.hs_out = nullptr;
     if (!set_pair_attrs(expert_gemm_pair_kernel<2>, sm)) return MOE_ERR_CUDA;
-    if (launch_pair(expert_gemm_pair_kernel<2>, grid, sm, st, tw, th, twsf, thsf, g) != MOE_OK) return MOE_ERR_CUDA;
+    if (launch_pair(expert_gemm_pair_kernel<2>, grid, sm, st, m, g) != MOE_OK) return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+// GEMM1 + GEMM2 + combine of a 208-token-tile problem in one launch on CTA
+// pairs (expert waves).  `sync`: 1 + max_token_tiles(P, E, 208) ints, zero on
+// entry.  Every CTA of the grid must be resident at once (one per SM).
+int launch_pair_fused(const moe_expert_args *a, uint16_t *y, int *sync, int *status, uint8_t *hq, uint8_t *sfb1,
+                      uint8_t *sfb2, const float *w_pool, const uint8_t *xq_pool, cudaStream_t st) {
+  const size_t sm = pair_smem_bytes(a->E);
+  const int grid = num_sms() & ~1;
+  PairMaps m{};
+  if (!encode_pair_maps(a, 0, xq_pool, sfb1, m) || !encode_pair_maps(a, 1, hq, sfb2, m)) return MOE_ERR_CUDA;
+  PairArgs g = pair_args(a, status, hq, sfb2, w_pool);
+  g.hs_out = nullptr;
+  g.sync = sync;
+  g.topk_idx = a->topk_idx;
+  g.y = reinterpret_cast<uint4 *>(y);
+  if (!set_pair_attrs(expert_gemm_pair_kernel<3>, sm)) return MOE_ERR_CUDA;
+  return launch_pair(expert_gemm_pair_kernel<3>, grid, sm, st, m, g);
+}
+
+// moe_forward's expert part for 208-token tiles: the single launch above on
+// the pool rows and token-scale chunks that the prep / cast kernel left in
+// the expert workspace `ews`.
+int launch_pair_layer(const moe_expert_args *a, uint16_t *y, int *sync, int *status, char *ews, cudaStream_t st) {
+  const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
+  uint8_t *hq = a->hq ? a->hq : reinterpret_cast<uint8_t *>(ews + lay.hq);
+  return launch_pair_fused(a, y, sync, status, hq, reinterpret_cast<uint8_t *>(ews + lay.sfb1),
+                           reinterpret_cast<uint8_t *>(ews + lay.sfb2), reinterpret_cast<const float *>(ews + lay.w_pool),
+                           reinterpret_cast<const uint8_t *>(ews + lay.xq_pool), st);
 }
 
 }  // namespace mxq

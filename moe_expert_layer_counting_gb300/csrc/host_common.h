@@ -132,6 +132,11 @@ int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logit
 // one M = 256 MMA (gemm2sm.cu).  Eligible when both GEMMs' 128-row weight
 // tiles pair up (2I/128 and H/128 even) and the shared memory fits.
 bool pair_eligible(int64_t H, int64_t I, int E);
+// moe_forward's large problems: GEMM1 + GEMM2 + combine in one launch on CTA
+// pairs (expert waves, 208-token tiles), after the pool rows and token-scale
+// chunks were written into the expert workspace `ews`; `sync` as for
+// launch_fused_gemms (zeroed before the launch).
+int launch_pair_layer(const moe_expert_args *a, uint16_t *y, int *sync, int *status, char *ews, cudaStream_t st);
 // The token tile a call uses: tile_n, or choose_tile_n's when 0; the large
 // tile is 208 tokens on CTA pairs (pair_eligible) and 224 on single CTAs.
 int resolve_tile_n(int tile_n, int64_t P, int64_t E, int64_t H, int64_t I);

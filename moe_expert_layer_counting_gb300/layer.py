@@ -46,12 +46,13 @@ class MoELayer:
     """The MoE expert layer for a fixed (max_tokens, H, I, E, k): y = layer(x, logits)."""
 
     def __init__(self, weights: QuantizedExperts, k: int, max_tokens: int, tile_n: int = 0,
-                 route_mode: int = B.ROUTE_SOFTMAX):
+                 route_mode: int = B.ROUTE_SOFTMAX, schedule: int = B.SCHEDULE_DEFAULT):
         self.w = weights
         self.k = k
         self.max_tokens = max_tokens
         self.tile_n = tile_n
         self.route_mode = route_mode
+        self.schedule = schedule
         nbytes = B.moe_workspace_size(max_tokens, weights.H, weights.I, weights.E, k)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=weights.w1q.device)
 
@@ -64,7 +65,7 @@ class MoELayer:
         ws = self.workspace
         need = B.moe_workspace_size(T, w.H, w.I, w.E, self.k)
         B.moe_forward(x, logits, w.w1q, w.w1s, w.w2q, w.w2s, self.k, y, ws[:need], tile_n=self.tile_n,
-                      route_mode=self.route_mode, stream=stream, **outs)
+                      route_mode=self.route_mode, schedule=self.schedule, stream=stream, **outs)
         return y
 
     def device_status(self, stream=None) -> int:

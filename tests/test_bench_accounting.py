@@ -43,12 +43,22 @@ def test_bfp8_small_decode_bytes_by_hand():
 
 def test_launches_per_forward():
     # small problems: front kernel + one launch of GEMM1 + GEMM2 + combine
-    assert bench.launches_per_forward(8, 2048, 256, 8) == 2
+    assert bench.launches_per_forward(8, 2048, 512, 256, 8) == 2
     assert bench.launches_per_forward_bfp8(8, 2048, 256, 8) == 2
-    # large decode: route, permute (one launch for <= 2048 pairs), cast, GEMM1, GEMM2, combine
+    # large decode (16-token tiles): route, permute (one launch for <= 2048 pairs), pool cast, GEMM1, GEMM2, combine
+    assert bench.launches_per_forward(128, 7168, 2048, 256, 8) == 6
     assert bench.launches_per_forward_bfp8(128, 7168, 256, 8) == 6
-    # prefill: quant, route, permute (count + scatter), pool prep, GEMM1, GEMM2, combine
-    assert bench.launches_per_forward(4096, 7168, 256, 8) == 8
+    # prefill (CTA pairs, default schedule): route, permute (count + scatter), quant, pool prep, GEMM1, GEMM2, combine
+    assert bench.launches_per_forward(4096, 7168, 2048, 256, 8) == 8
+    # ... under the expert-wave schedule: GEMM1 + GEMM2 + combine in one launch
+    assert bench.launches_per_forward(4096, 7168, 2048, 256, 8, schedule=2) == 6
+    assert bench.single_gemm_launch(4096, 7168, 2048, 256, 8, schedule=2)
+    assert not bench.single_gemm_launch(4096, 7168, 2048, 256, 8)
+    assert bench.single_gemm_launch(8, 2048, 512, 256, 8)
+    assert not bench.single_gemm_launch(128, 7168, 2048, 256, 8, schedule=2)
+    # H/128 odd: one-CTA 224-token tiles, separate GEMM launches
+    assert not bench.pair_tiles(4096, 7168 - 128, 2048, 256, 8)
+    assert not bench.single_gemm_launch(4096, 7168 - 128, 2048, 256, 8, schedule=2)
 
 
 def test_layer_rates():

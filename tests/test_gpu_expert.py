@@ -149,7 +149,7 @@ def test_expert_forward_small_decode(B):
         _compare_pairs(st, y_g, hq_g, hs_g, y_ref, hq_ref, hs_ref, f"small_decode tile_n={tile_n}")
 
 
-def _forward(B, st, tile_n=0):
+def _forward(B, st, tile_n=0, schedule=0):
     wl = st.wl
     dev = "cuda"
     y = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
@@ -161,7 +161,7 @@ def _forward(B, st, tile_n=0):
     ws = torch.empty(B.moe_workspace_size(wl.T, wl.H, wl.I, wl.E, wl.k), dtype=torch.uint8, device=dev)
     B.moe_forward(st.x.cuda(), st.logits.cuda(), st.qe.w1q, st.qe.w1s, st.qe.w2q, st.qe.w2s, wl.k, y, ws,
                   topk_idx_out=idx, topk_w_out=w, counts_out=counts, offsets_out=offsets, perm_out=perm,
-                  tile_n=tile_n)
+                  tile_n=tile_n, schedule=schedule)
     torch.cuda.synchronize()
     assert B.moe_get_device_status(ws) == 0
     assert np.array_equal(idx.cpu().numpy(), st.idx_ref)
@@ -197,15 +197,17 @@ def pool():
         yield p
 
 
-@pytest.mark.parametrize("wl_name", ["large_decode", "prefill", "skewed_prefill"])
-def test_large_workloads_sampled(B, pool, wl_name):
+@pytest.mark.parametrize("wl_name,schedule", [("large_decode", 0), ("prefill", 0), ("skewed_prefill", 0),
+                                              ("skewed_prefill", 2)])
+def test_large_workloads_sampled(B, pool, wl_name, schedule):
     """The large workloads through moe_forward at full size.
 
     * routing, counts, offsets and perm: bit-exact on every token (in _forward);
     * y of a seeded sample of tokens (the first and last tokens of the two
       hottest and the two coldest non-empty experts, the last tokens of
       expert 0, random ones) against the oracle's layer run on those tokens
-      with its own cast, routing and weights;
+      with its own cast, routing and weights (schedule 2: the prefill
+      workloads' GEMMs and combine as one expert-wave launch);
     * per-pair rows and h of a sample of experts (moe_expert_forward);
     * y of every token against the oracle's combine of the GPU's own
       per-pair rows (computed with the layer's routing weights)."""
@@ -218,7 +220,7 @@ def test_large_workloads_sampled(B, pool, wl_name):
     need = sorted(set(experts) | set(int(e) for e in idx_ref[toks].reshape(-1)))
     st = Setup(B, wl, oracle_experts=need, weight_device="cuda", pool=pool)
     st.check_weights_bitexact()
-    y_fwd, w_dev = _forward(B, st)
+    y_fwd, w_dev = _forward(B, st, schedule=schedule)
     # sampled tokens: moe_forward's rows against the oracle's layer
     ref = Hp.oracle_forward_tokens(pool, Hp.bits16(x)[toks], logits.numpy()[toks], st.oracle_weights(), wl.k)
     assert np.array_equal(ref["topk_idx"], st.idx_ref[toks])

@@ -20,14 +20,14 @@ pytestmark = pytest.mark.gpu
 WAIT_SITE_INJECTED = 7
 
 
-def _tiny(tile_n=0):
+def _tiny(tile_n=0, wl=None, schedule=0):
     import workloads as W
     from moe_expert_layer_counting_gb300.layer import MoELayer, QuantizedExperts
-    wl = W.WORKLOADS["tiny"]
+    wl = wl or W.WORKLOADS["tiny"]
     x, logits = W.tokens(wl)
     l1, l2 = W.all_expert_weights(wl, "cpu")
     qe = QuantizedExperts.from_bf16(l1.cuda(), l2.cuda())
-    return wl, x, logits, l1, l2, MoELayer(qe, wl.k, wl.T, tile_n=tile_n)
+    return wl, x, logits, l1, l2, MoELayer(qe, wl.k, wl.T, tile_n=tile_n, schedule=schedule)
 
 
 def _oracle_y(wl, x, logits, l1, l2):
@@ -40,18 +40,26 @@ def _oracle_y(wl, x, logits, l1, l2):
     return O.forward(bits(x), logits.numpy(), w1q, w1s, w2q, w2s, wl.k)["y"]
 
 
-@pytest.mark.parametrize("tile_n", [16, 32, 224])
-def test_injected_wait_times_out_then_recovers(monkeypatch, tile_n):
-    """tile_n 16: GEMM1 + GEMM2 + combine in one launch (CTAs also wait on
-    one another's arrival counters); 32: separate GEMM launches; 224: the
-    GEMMs on CTA pairs (the leader's MMA issuer takes the injected wait, the
-    other CTA of each pair must give up through the abort flag)."""
+@pytest.mark.parametrize("case", ["tile16", "tile32", "pairs", "pair_layer"])
+def test_injected_wait_times_out_then_recovers(monkeypatch, case):
+    """tile16: GEMM1 + GEMM2 + combine in one launch (CTAs also wait on one
+    another's arrival counters); tile32: separate GEMM launches; pairs: the
+    GEMMs on CTA pairs as separate launches (the leader's MMA issuers take the
+    injected wait, the other CTA of each pair must give up through the abort
+    flag); pair_layer: a larger problem whose GEMM1 + GEMM2 + combine run in
+    one launch on CTA pairs under the expert-wave schedule (GEMM2 items also
+    wait on arrival counters)."""
     from helpers import lib
     lib()
+    import workloads as W
     from moe_expert_layer_counting_gb300 import binding as B
     from oracle import formats as F
 
-    wl, x, logits, l1, l2, layer = _tiny(tile_n)
+    if case == "pair_layer":
+        wl = W.Workload("pair_layer", T=700, H=512, I=256, E=6, k=2, sigma=0.02, seed=21)
+        wl, x, logits, l1, l2, layer = _tiny(0, wl, schedule=2)
+    else:
+        wl, x, logits, l1, l2, layer = _tiny({"tile16": 16, "tile32": 32, "pairs": 224}[case])
     xd, ld = x.cuda(), logits.cuda()
     layer(xd, ld)                                  # warm-up (module load, tensor maps)
     torch.cuda.synchronize()

@@ -43,12 +43,15 @@ def B():
     return Hp.lib()
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
-def test_forward_shape(B, name):
+@pytest.mark.parametrize("name,schedule", [(n, 0) for n in SHAPES] +
+                         [(n, 2) for n in ("large_path", "pair_ragged", "pair_two_sf_groups", "pair_fallback")])
+def test_forward_shape(B, name, schedule):
+    """schedule 2: the expert-wave single launch where the shape runs on CTA
+    pairs (the one-CTA fallback ignores it)."""
     T, H, I, E, k = SHAPES[name]
     wl = W.Workload(name, T=T, H=H, I=I, E=E, k=k, sigma=0.02, seed=11 + len(name))
     st = Setup(B, wl, weight_device="cuda")
-    y_g, _ = _forward(B, st)
+    y_g, _ = _forward(B, st, schedule=schedule)
     ref = O.forward(Hp.bits16(st.x), st.logits.numpy(), st.w1q_ref, st.w1s_ref, st.w2q_ref, st.w2s_ref, k)
     Hp.assert_bf16_close(y_g, ref["y"], what=name)
     if k == 1:
