@@ -54,9 +54,15 @@ WORKLOADS = {
 }
 
 # Smaller cases with the same per-expert shapes, for profiler captures that
-# must stay small (the prefill's ~128 pairs per expert on 32 experts).
+# must stay small: the prefill's ~128 pairs per expert on 32 experts, the
+# skewed prefill's popularity on 64 experts (hot experts of ~2000 pairs, i.e.
+# ten 208-token tiles, a few experts with fewer than ten pairs; 1.5 GB of
+# weights instead of 6).
 PROFILE_WORKLOADS = {
     "prefill_e32": Workload("prefill_e32", T=512, H=7168, I=2048, E=32, k=8, sigma=0.01, seed=3),
+    "skewed_e64": Workload("skewed_e64", T=2048, H=7168, I=2048, E=64, k=8, sigma=0.01, seed=4, zipf_s=1.2),
+    # the large decode's ~4 pairs per expert on 32 experts (0.75 GB of weights)
+    "large_decode_e32": Workload("large_decode_e32", T=16, H=7168, I=2048, E=32, k=8, sigma=0.01, seed=2),
 }
 
 
