@@ -51,19 +51,23 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM GB/s)"
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
-# GEMM phase alone (the launch the roofline times), from one-pass ncu captures
-# (ncu flushes the caches before each captured launch) of the GEMM kernel
-# built from sources whose SHA-256 is `src_sha256`
-# (commands and figures in profiles/).  `traffic` is reported as null once
-# those sources change.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# GEMM launches, from one-pass ncu captures (ncu flushes the caches before
+# each captured launch) of the kernels built from sources whose SHA-256 is
+# `src_sha256` (commands and figures in profiles/dram_traffic_gemm.md).  The
+# prefills were captured on smaller cases with the same per-expert shapes
+# (workloads.PROFILE_WORKLOADS) and enter as the ratio of measured to
+# algorithmic bytes of that case, applied to the full workload's algorithmic
+# bytes; the small decode was captured at full size.  `traffic` is reported
+# as null once those sources change or for launches not captured.
 GEMM_SOURCES = ("gemm.cu", "gemm2sm.cu", "gemm_common.cuh", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC = {
-    "src_sha256": "34049e5ab0ee6b69086c8a0d5539f70af5e8ef42ab113637067f39a5008b6996",
-    "small_decode": {"gemm1": 62794496 + 2048, "gemm2": 31327744 + 0},
-    "large_decode": {"gemm1": 3959589888 + 2434816, "gemm2": 1976362752 + 14259968},
-    "prefill": {"gemm1": 4272065792 + 67646464, "gemm2": 2068049920 + 449129472},
-    "skewed_prefill": {"gemm1": 3272554240 + 140031744, "gemm2": 1335592960 + 939598336},
+    "src_sha256": "a6ca8e41174df8f7a674c868752c793949fb1e9010847fc85b9855b5a66a9fc1",
+    "small_decode": {"fused": {"bytes": 94066688 + 1773568, "from": "small_decode (full size)"}},
+    "prefill": {"gemm1": {"ratio": (532804608 + 8838656) / 511557632, "from": "prefill_e32"},
+                "gemm2": {"ratio": (258569728 + 38214400) / 316932096, "from": "prefill_e32"}},
+    "skewed_prefill": {"gemm1": {"ratio": (1130601216 + 37796608) / 1047986176, "from": "skewed_e64"},
+                       "gemm2": {"ratio": (534896640 + 233217792) / 768606208, "from": "skewed_e64"}},
 }
 # the same for the block-FP8 variant's GEMMs (csrc/bfp8.cu)
 BFP8_SOURCES = ("bfp8.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
@@ -174,13 +178,19 @@ def gemm_sources_sha256(sources=GEMM_SOURCES):
     return h.hexdigest()
 
 
-def measured_traffic(workload, phase, bfp8=False):
-    """Bytes per launch from the ncu tables above, or None if stale or not captured."""
+def measured_traffic(workload, phase, alg_bytes, bfp8=False):
+    """(bytes per launch, how) from the ncu tables above, or (None, why) if stale or not captured."""
     table, sources = (TRAFFIC_BFP8, BFP8_SOURCES) if bfp8 else (TRAFFIC, GEMM_SOURCES)
-    entry = table.get(workload, {})
-    if table.get("src_sha256") != gemm_sources_sha256(sources) or phase not in entry:
-        return None
-    return entry[phase]
+    if table.get("src_sha256") != gemm_sources_sha256(sources):
+        return None, "kernel sources changed since the capture"
+    entry = table.get(workload, {}).get(phase)
+    if entry is None:
+        return None, "not captured"
+    if isinstance(entry, dict) and "ratio" in entry:
+        return int(round(entry["ratio"] * alg_bytes)), f"scaled from {entry['from']} (measured / algorithmic = {entry['ratio']:.4f})"
+    if isinstance(entry, dict):
+        return entry["bytes"], f"measured on {entry['from']}"
+    return entry, "measured at full size"
 
 
 def peaks():
@@ -437,9 +447,11 @@ def measure(args, wl, dev, stream, world, rank, headline):
     else:
         dom = "gemm1" if g1 >= g2 else "gemm2"
         dom_ms = max(g1, g2)
-        what = f"{kname} ({dom}, one launch)"
+        what = (f"expert_gemm_pair_kernel ({dom}, one launch, CTA pairs)" if (not bfp8 and pair_tiles(T, H, I, E, k))
+                else f"{kname} ({dom}, one launch)")
     roof = roofline_of(alg, dom, dom_ms, hbm, fp8_peak_tflops)
-    roof.update({"kernel": what, "ms": round(dom_ms, 5), "traffic": measured_traffic(wl.name, dom, bfp8),
+    traffic, traffic_how = measured_traffic(wl.name, dom, roof["algorithmic_bytes"], bfp8)
+    roof.update({"kernel": what, "ms": round(dom_ms, 5), "traffic": traffic, "traffic_source": traffic_how,
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)"})
     layer_time_bound = max(alg["layer_bytes"] / (hbm * 1e9), alg["layer_flops"] / (fp8_peak_tflops * 1e12))
     out = {
