@@ -733,7 +733,7 @@ def launches_per_forward(T, H, I, E, k, schedule=0):
         if -(-P // ne) <= 16:                  # 16-token tiles
             return 2                           # front (route + permute + pool cast), GEMM1 + GEMM2 + combine
         return 4                               # front, GEMM1, GEMM2, combine
-    cast = 1 if P * H <= (16 << 20) else 2     # pool cast, or activation cast + pool copy
+    cast = 1                                   # pool-order cast, or token-order cast (P*H > 16M)
     if single_gemm_launch(T, H, I, E, k, schedule):
         return 1 + permute + cast + 1          # route, permute, cast, GEMM1 + GEMM2 + combine
     return 1 + permute + cast + 3              # route, permute, cast, GEMM1, GEMM2, combine

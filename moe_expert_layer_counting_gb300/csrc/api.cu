@@ -70,7 +70,7 @@ constexpr int64_t kPoolCastMaxValues = int64_t(16) << 20;
 
 struct ForwardWs {
   size_t sync_end;   // status words, then the single-launch layer's arrival counters (zeroed per call)
-  size_t xq, xs, idx, w, counts, offsets, perm, inv_perm, perm_scratch, expert, y_pairs, total;
+  size_t idx, w, counts, offsets, perm, inv_perm, perm_scratch, expert, y_pairs, total;
 };
 
 ForwardWs forward_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
@@ -79,8 +79,6 @@ ForwardWs forward_ws_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   size_t off = kStatusBytes;
   off += round_up(fused_sync_ints(T, (int)E, (int)k) * 4, 256);
   w.sync_end = off;
-  w.xq = off;           off += round_up((size_t)T * H, 256);
-  w.xs = off;           off += round_up((size_t)T * (H / 32), 256);
   w.idx = off;          off += round_up((size_t)P * 4, 256);
   w.w = off;            off += round_up((size_t)P * 4, 256);
   w.counts = off;       off += round_up((size_t)E * 4, 256);
@@ -122,8 +120,10 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   moe_expert_args ea{};
   ea.struct_size = sizeof(moe_expert_args);
   ea.T = a->T; ea.H = a->H; ea.I = a->I; ea.E = a->E; ea.k = a->k;
-  ea.xq = reinterpret_cast<uint8_t *>(ws + lay.xq);
-  ea.xs = reinterpret_cast<uint8_t *>(ws + lay.xs);
+  // every front end casts x straight into the pool rows (no token-order copy)
+  ea.xq = nullptr;
+  ea.xs = nullptr;
+  ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
   ea.w1q = a->w1q; ea.w1s = a->w1s; ea.w2q = a->w2q; ea.w2s = a->w2s;
   int32_t *idx = a->topk_idx_out ? a->topk_idx_out : reinterpret_cast<int32_t *>(ws + lay.idx);
   float *wts = a->topk_w_out ? a->topk_w_out : reinterpret_cast<float *>(ws + lay.w);
@@ -180,7 +180,6 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
     // then, with 16-token tiles, both GEMMs and the combine in one more
     if (fused)
       return launch_fused_gemms(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
-    ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
     rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
     if (rc != MOE_OK) return rc;
     return launch_combine(ea.y_pairs, idx, a->T, a->k, a->H, a->y, st);
@@ -193,25 +192,14 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
     // small problems: cast x straight into GEMM1's pool rows and scale chunks
     // (one launch, every load in flight at once)
     rc = launch_pool_cast(&ea, a->x, ws + lay.expert, st);
-    if (rc != MOE_OK) return rc;
-    ea.phases = MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2;
   } else {
-    // large problems: cast each token once, then copy FP8 rows into pool order
-    // (half the bytes of re-reading BF16 rows k times)
-    rc = launch_quant_act(a->x, a->T, a->H, const_cast<uint8_t *>(ea.xq), const_cast<uint8_t *>(ea.xs), st);
-    if (rc != MOE_OK) return rc;
-    ea.phases = 0;
+    // large problems: cast each token once (x read once) and scatter its codes
+    // to its k pool rows
+    rc = launch_token_cast(&ea, a->x, inv_perm, ws + lay.expert, st);
   }
-  if (pair_layer) {
-    // the pool rows (prep step, if the cast above did not write them), then
-    // both GEMMs and the combine in one launch
-    if (ea.phases == 0) {
-      ea.phases = MOE_PHASE_TOKEN_SCALES;
-      rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
-      if (rc != MOE_OK) return rc;
-    }
+  if (rc != MOE_OK) return rc;
+  if (pair_layer)   // both GEMMs and the combine in one launch
     return launch_pair_layer(&ea, a->y, status + kStatusBytes / 4, status, ws + lay.expert, st);
-  }
   rc = launch_expert_forward(&ea, status, ws + lay.expert, st);
   if (rc != MOE_OK) return rc;
   return launch_combine(ea.y_pairs, idx, a->T, a->k, a->H, a->y, st);

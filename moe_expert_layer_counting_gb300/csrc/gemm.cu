@@ -656,6 +656,93 @@ __global__ void __launch_bounds__(256) pool_cast_kernel(const uint4 *__restrict_
   }
 }
 
+// The activation cast of large problems, in token order: a warp per token
+// reads its BF16 row once (a pool-order cast re-reads it k times, from DRAM
+// once x outgrows L2), casts it to E4M3 with one UE8M0 scale per 32 values and
+// writes the codes to the pool rows of the token's k pairs
+// (s = inv_perm[t*k + j]; -1 = dropped pair).  Lanes 0..k-1 first locate
+// their pair's pool row and scale-chunk position (one search per pair, not
+// per value), which the column loop then takes by shuffle.  Per 256-value
+// step a lane casts 8 values (four lanes form a 32-group, as pool_cast_kernel)
+// and the first lane of each 16 writes the four scale bytes of its 128-value
+// K block as one word; four steps' loads are issued before the first cast.
+constexpr int kTokenCastUnroll = 4;
+
+template <int BN>
+__global__ void __launch_bounds__(256) token_cast_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ counts,
+                                                         const int32_t *__restrict__ offsets,
+                                                         const int32_t *__restrict__ inv_perm,
+                                                         const float *__restrict__ topk_w, int64_t T, int E, int k,
+                                                         int H, uint8_t *__restrict__ chunks,
+                                                         int32_t *__restrict__ tok_pool, float *__restrict__ w_pool,
+                                                         uint2 *__restrict__ xq_pool) {
+  extern __shared__ int sh[];
+  int *tile_off = sh, *cnt_sm = sh + (E + 1), *off_sm = sh + 2 * (E + 1);
+  pdl_launch_dependents();
+  pdl_wait();
+  load_expert_table(counts, offsets, E, cnt_sm, off_sm);
+  __syncthreads();
+  __shared__ int scan_scratch[9];
+  block_tile_map<256>(cnt_sm, E, BN, tile_off, scan_scratch, scan_scratch + 8);
+  __syncthreads();
+  const int H8 = H / 8, KB = H / 128;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+    // lane j < k (k <= 32): pool row of pair (t, j) and the offset of its
+    // scale word in K block 0
+    int s_mine = -1;
+    int64_t sfo_mine = 0;
+    if (lane < k) {
+      const int64_t p = t * k + lane;
+      s_mine = __ldg(inv_perm + p);
+      if (s_mine >= 0) {
+        int lo = 0, hi = E;                      // expert e with off[e] <= s < off[e+1]
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (off_sm[mid] <= s_mine) lo = mid; else hi = mid;
+        }
+        const int rank = s_mine - off_sm[lo];
+        const int g = tile_off[lo] + rank / BN, r = rank % BN;
+        const int rr = r & 127;
+        sfo_mine = (int64_t)g * KB * Cfg<BN>::kTokChunk + (r >> 7) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
+        tok_pool[s_mine] = (int32_t)t;
+        w_pool[s_mine] = __ldg(topk_w + p);
+      }
+    }
+    const uint4 *xrow = x + t * H8;
+    for (int c0 = 0; c0 < H8; c0 += 32 * kTokenCastUnroll) {
+      uint4 v[kTokenCastUnroll];
+#pragma unroll
+      for (int u = 0; u < kTokenCastUnroll; ++u) {
+        const int c = c0 + 32 * u + lane;
+        v[u] = c < H8 ? __ldg(xrow + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kTokenCastUnroll; ++u) {
+        const int cb = c0 + 32 * u;              // warp-uniform
+        if (cb >= H8) break;
+        const int c = cb + lane;
+        const bool valid = c < H8;               // uniform over each 16 lanes (H8 % 16 == 0)
+        uint8_t sb;
+        const uint2 codes = cast8_e4m3(v[u], valid, &sb);
+        uint32_t word = sb;                      // meaningful in lanes with c % 16 == 0
+        word |= __shfl_down_sync(0xffffffffu, (uint32_t)sb, 4) << 8;
+        word |= __shfl_down_sync(0xffffffffu, (uint32_t)sb, 8) << 16;
+        word |= __shfl_down_sync(0xffffffffu, (uint32_t)sb, 12) << 24;
+        const int64_t kb_off = (int64_t)(c >> 4) * Cfg<BN>::kTokChunk;
+        for (int j = 0; j < k; ++j) {
+          const int s = __shfl_sync(0xffffffffu, s_mine, j);
+          const int64_t sfo = __shfl_sync(0xffffffffu, sfo_mine, j);
+          if (s < 0 || !valid) continue;
+          xq_pool[(size_t)s * H8 + c] = codes;
+          if ((c & 15) == 0) *reinterpret_cast<uint32_t *>(chunks + sfo + kb_off) = word;
+        }
+      }
+    }
+  }
+}
+
 // Small problems in one launch.  Every CTA routes all T tokens and builds the
 // whole counting-sort permutation in shared memory -- the same result in every
 // CTA, so no grid-wide synchronisation is needed -- CTA 0 writes the routing
@@ -813,6 +900,19 @@ int launch_pool_cast_t(const moe_expert_args *a, const uint16_t *x, char *ws, co
                     reinterpret_cast<float *>(ws + lay.w_pool), reinterpret_cast<uint2 *>(ws + lay.xq_pool));
 }
 
+template <int BN>
+int launch_token_cast_t(const moe_expert_args *a, const uint16_t *x, const int32_t *inv_perm, char *ws,
+                        const ExpertWs &lay, cudaStream_t st) {
+  const size_t sm = (size_t)3 * (a->E + 1) * 4;
+  const int64_t blocks = ceil_div(a->T, 8);                  // a warp per token
+  const int cap = num_sms() * 8;
+  const int grid = (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+  return launch_pdl(token_cast_kernel<BN>, dim3(grid), dim3(256), sm, st, reinterpret_cast<const uint4 *>(x),
+                    a->counts, a->offsets, inv_perm, a->topk_w, a->T, a->E, a->k, (int)a->H,
+                    reinterpret_cast<uint8_t *>(ws + lay.sfb1), reinterpret_cast<int32_t *>(ws + lay.tok_pool),
+                    reinterpret_cast<float *>(ws + lay.w_pool), reinterpret_cast<uint2 *>(ws + lay.xq_pool));
+}
+
 template <int BN, bool FROM_TOKENS>
 int launch_prep(const uint8_t *src, const moe_expert_args *a, int KB, uint8_t *chunks, int32_t *tok_pool,
                 float *w_pool, uint8_t *xq_pool, cudaStream_t st) {
@@ -922,6 +1022,23 @@ int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch,
     case 128: return launch_pool_cast_t<128>(a, x, ws, lay, st);
     case 208: return launch_pool_cast_t<208>(a, x, ws, lay, st);
     case 224: return launch_pool_cast_t<224>(a, x, ws, lay, st);
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
+int launch_token_cast(const moe_expert_args *a, const uint16_t *x, const int32_t *inv_perm, void *scratch,
+                      cudaStream_t st) {
+  const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
+  if (a->T == 0) return MOE_OK;
+  char *ws = reinterpret_cast<char *>(scratch);
+  const int bn = resolve_tile_n(a->tile_n, a->T * a->k, a->E, a->H, a->I);
+  switch (bn) {
+    case 16: return launch_token_cast_t<16>(a, x, inv_perm, ws, lay, st);
+    case 32: return launch_token_cast_t<32>(a, x, inv_perm, ws, lay, st);
+    case 64: return launch_token_cast_t<64>(a, x, inv_perm, ws, lay, st);
+    case 128: return launch_token_cast_t<128>(a, x, inv_perm, ws, lay, st);
+    case 208: return launch_token_cast_t<208>(a, x, inv_perm, ws, lay, st);
+    case 224: return launch_token_cast_t<224>(a, x, inv_perm, ws, lay, st);
     default: return MOE_ERR_INVALID_ARG;
   }
 }
@@ -1043,12 +1160,14 @@ int check_expert_args(const moe_expert_args *a, bool need_ws) {
       return MOE_ERR_WORKSPACE_TOO_SMALL;
   }
   if (a->T == 0) return MOE_OK;
-  if (!a->xq || !a->xs || !a->w1q || !a->w1s || !a->w2q || !a->w2s || !a->topk_idx || !a->topk_w || !a->counts ||
-      !a->offsets || !a->perm || !a->y_pairs)
+  // the token step (phases 0 includes it) reads xq / xs
+  const bool token_step = a->phases == 0 || (a->phases & MOE_PHASE_TOKEN_SCALES);
+  if ((token_step && (!a->xq || !a->xs)) || !a->w1q || !a->w1s || !a->w2q || !a->w2s || !a->topk_idx ||
+      !a->topk_w || !a->counts || !a->offsets || !a->perm || !a->y_pairs)
     return MOE_ERR_INVALID_ARG;
   if (!aligned(a->w1q, 32) || !aligned(a->w2q, 32)) return MOE_ERR_MISALIGNED;
-  if (!aligned(a->xq, 16) || !aligned(a->xs, 16) || !aligned(a->w1s, 16) || !aligned(a->w2s, 16) ||
-      !aligned(a->y_pairs, 16) || (a->hq && !aligned(a->hq, 16)))
+  if ((token_step && (!aligned(a->xq, 16) || !aligned(a->xs, 16))) || !aligned(a->w1s, 16) ||
+      !aligned(a->w2s, 16) || !aligned(a->y_pairs, 16) || (a->hq && !aligned(a->hq, 16)))
     return MOE_ERR_MISALIGNED;
   return MOE_OK;
 }

@@ -27,7 +27,8 @@
 //   * all waits are bounded (MOE_ERR_TIMEOUT in the status words); the pair
 //     meets at a cluster barrier before TMEM is freed, so no CTA exits while
 //     the other still reads its shared memory or signals its barriers.
-// Work order: expert-major, then weight-row pair, then token tile (as gemm.cu).
+// Work order of the separate launches: token tiles in zigzag order over the
+// expert-ordered tile list, the weight-row pairs of a tile fastest.
 #include <cuda_bf16.h>
 
 #include <cstdlib>
@@ -145,10 +146,15 @@ __device__ __forceinline__ PairItem decode_pair_item(int w, const PairArgs &args
   PairItem it;
   int g;
   if (PHASE != 3) {
+    // separate launches: tiles in zigzag order (0, NT-1, 1, NT-2, ...), so that
+    // the many-token tiles of popular experts (compute-heavy) and the
+    // few-token tiles of rare experts (weight-streaming) are in flight together
+    // (skewed prefill: -1.2 % per GEMM, measured; uniform routing: no change)
     const int MT2 = args.MT[PHASE - 1] >> 1;
     it.gemm = PHASE - 1;
-    g = w / MT2;
-    it.ti.mt = w - g * MT2;
+    const int gi = w / MT2;
+    it.ti.mt = w - gi * MT2;
+    g = (gi & 1) ? NT - 1 - (gi >> 1) : (gi >> 1);
   } else {
     const int m1 = args.MT[0] >> 1, m2 = args.MT[1] >> 1;
     const int nw = (NT + kWaveTiles - 1) / kWaveTiles;          // waves

@@ -115,6 +115,10 @@ int launch_expert_forward(const moe_expert_args *a, int *status, void *scratch, 
 // Activation cast straight into GEMM1's pool rows and scale chunks (replaces
 // mxq_quantize_act + the token-scale step inside moe_forward).
 int launch_pool_cast(const moe_expert_args *a, const uint16_t *x, void *scratch, cudaStream_t st);
+// Large problems: the activation cast in token order, each BF16 row read once
+// and written to its k pool rows + scale chunks (inv_perm from moe_permute).
+int launch_token_cast(const moe_expert_args *a, const uint16_t *x, const int32_t *inv_perm, void *scratch,
+                      cudaStream_t st);
 // Small problems (front_eligible): routing, counting-sort permute and the pool
 // cast in one launch.  `a` supplies shapes, tile size and the counts / offsets /
 // perm outputs.

@@ -48,10 +48,10 @@ def test_launches_per_forward():
     # large decode (16-token tiles): route, permute (one launch for <= 2048 pairs), pool cast, GEMM1, GEMM2, combine
     assert bench.launches_per_forward(128, 7168, 2048, 256, 8) == 6
     assert bench.launches_per_forward_bfp8(128, 7168, 256, 8) == 6
-    # prefill (CTA pairs, default schedule): route, permute (count + scatter), quant, pool prep, GEMM1, GEMM2, combine
-    assert bench.launches_per_forward(4096, 7168, 2048, 256, 8) == 8
+    # prefill (CTA pairs, default schedule): route, permute (count + scatter), token-order cast, GEMM1, GEMM2, combine
+    assert bench.launches_per_forward(4096, 7168, 2048, 256, 8) == 7
     # ... under the expert-wave schedule: GEMM1 + GEMM2 + combine in one launch
-    assert bench.launches_per_forward(4096, 7168, 2048, 256, 8, schedule=2) == 6
+    assert bench.launches_per_forward(4096, 7168, 2048, 256, 8, schedule=2) == 5
     assert bench.single_gemm_launch(4096, 7168, 2048, 256, 8, schedule=2)
     assert not bench.single_gemm_launch(4096, 7168, 2048, 256, 8)
     assert bench.single_gemm_launch(8, 2048, 512, 256, 8)

@@ -3,8 +3,8 @@ with the oracle.
 
 moe_forward picks one of three front ends from the problem size: the fused
 small-problem kernel (T <= 64, E <= 256, T*k*H <= 4M), routing + permute + a
-pool cast (P*H <= 16M), or routing + permute + activation cast + pool copy
-(larger), and the token tile from the mean pairs per routed expert; 224-token
+pool-order cast (P*H <= 16M), or routing + permute + a token-order cast that
+writes each token's codes to its k pool rows (larger), and the token tile from the mean pairs per routed expert; 224-token
 tiles run on CTA pairs where the weight tiles pair up.  The
 shapes below are small enough for the float64 oracle, with ragged counts,
 E not a multiple of 32, a single token, k = 1, and a few thousand pairs."""
@@ -27,7 +27,8 @@ SHAPES = {
     "k1": (40, 512, 256, 10, 1),                # front kernel, k = 1 (weight 1)
     "pool_cast": (100, 256, 128, 24, 4),        # T > 64: routing + permute + pool cast
     "wide_H_front": (3, 7168, 128, 9, 2),       # front kernel, 224 column groups
-    "large_path": (2048, 1024, 128, 64, 8),     # P*H > 16M: activation cast + pool copy, 224-token tiles
+    "large_path": (2048, 1024, 128, 64, 8),     # P*H > 16M: token-order cast, 224-token tiles
+    "token_cast_odd_H": (2000, 1152, 128, 40, 8),   # token-order cast, H/8 = 144: a half-warp last step; H/128 odd: one-CTA 224 tiles
     "one_expert": (40, 256, 128, 1, 1),         # front kernel, E = 1, k = 1: three token tiles of one expert
     # 224-token tiles on CTA pairs (weight tiles pair up: 2I/128 and H/128 even)
     "pair_ragged": (700, 512, 256, 6, 2),       # ~233 pairs per expert: one or two tiles, ragged last tile
