@@ -60,14 +60,24 @@ METRIC = "MoE-layer tokens/s on 1 GB300; % of roofline (FP8 tensor peak or HBM G
 # algorithmic bytes of that case, applied to the full workload's algorithmic
 # bytes; the small decode was captured at full size.  `traffic` is reported
 # as null once those sources change or for launches not captured.
-GEMM_SOURCES = ("gemm.cu", "gemm2sm.cu", "gemm_common.cuh", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
+PAIR_SOURCES = ("gemm2sm.cu", "gemm_common.cuh", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
+ONE_CTA_SOURCES = ("gemm.cu", "gemm_common.cuh", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC = {
-    "src_sha256": "a6ca8e41174df8f7a674c868752c793949fb1e9010847fc85b9855b5a66a9fc1",
-    "small_decode": {"fused": {"bytes": 94066688 + 1773568, "from": "small_decode (full size)"}},
-    "prefill": {"gemm1": {"ratio": (532804608 + 8838656) / 511557632, "from": "prefill_e32"},
-                "gemm2": {"ratio": (258569728 + 38214400) / 316932096, "from": "prefill_e32"}},
-    "skewed_prefill": {"gemm1": {"ratio": (1130601216 + 37796608) / 1047986176, "from": "skewed_e64"},
-                       "gemm2": {"ratio": (534896640 + 233217792) / 768606208, "from": "skewed_e64"}},
+    # the CTA-pair kernel (208-token tiles)
+    "pair": {
+        "sources": PAIR_SOURCES,
+        "src_sha256": "36baa69fe10f4e84f1dbae6e9075efed2e9bc641092c25ef21c5bfb5025b102f",
+        "prefill": {"gemm1": {"ratio": (533717248 + 8354304) / 511557632, "from": "prefill_e32"},
+                    "gemm2": {"ratio": (258542336 + 38179072) / 316932096, "from": "prefill_e32"}},
+        "skewed_prefill": {"gemm1": {"ratio": (1195241216 + 33373952) / 1047986176, "from": "skewed_e64"},
+                           "gemm2": {"ratio": (535361536 + 196535296) / 768606208, "from": "skewed_e64"}},
+    },
+    # the one-CTA kernel (small tiles; the small decode's fused launch)
+    "one_cta": {
+        "sources": ONE_CTA_SOURCES,
+        "src_sha256": "b6b740adc635142926e2264a069ebd6c3414e6ac6a7d398d145f86f1a4f9a042",
+        "small_decode": {"fused": {"bytes": 94066688 + 1773568, "from": "small_decode (full size)"}},
+    },
 }
 # the same for the block-FP8 variant's GEMMs (csrc/bfp8.cu)
 BFP8_SOURCES = ("bfp8.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
@@ -168,7 +178,7 @@ def gpu_id_for(dev) -> str:
 
 # ---------------------------------------------------------------- roofline bookkeeping
 
-def gemm_sources_sha256(sources=GEMM_SOURCES):
+def gemm_sources_sha256(sources):
     import hashlib
     h = hashlib.sha256()
     base = os.path.join(os.path.dirname(os.path.abspath(__file__)), "moe_expert_layer_counting_gb300", "csrc")
@@ -180,7 +190,13 @@ def gemm_sources_sha256(sources=GEMM_SOURCES):
 
 def measured_traffic(workload, phase, alg_bytes, bfp8=False):
     """(bytes per launch, how) from the ncu tables above, or (None, why) if stale or not captured."""
-    table, sources = (TRAFFIC_BFP8, BFP8_SOURCES) if bfp8 else (TRAFFIC, GEMM_SOURCES)
+    if bfp8:
+        table, sources = TRAFFIC_BFP8, BFP8_SOURCES
+    else:
+        table = next((f for f in TRAFFIC.values() if phase in f.get(workload, {})), None)
+        if table is None:
+            return None, "not captured"
+        sources = table["sources"]
     if table.get("src_sha256") != gemm_sources_sha256(sources):
         return None, "kernel sources changed since the capture"
     entry = table.get(workload, {}).get(phase)

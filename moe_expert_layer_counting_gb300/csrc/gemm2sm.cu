@@ -51,7 +51,10 @@ struct Pair {
   static constexpr int kStages = kStreams * kStagesPerStream;
   static constexpr int kEpiWarps = 16;                    // four groups of four (one TMEM lane quadrant each)
   static constexpr int kEpiGroups = kEpiWarps / 4;
-  static constexpr int kFirstEpiWarp = 2 * kStreams;      // warps 0-1 producers, 2-3 MMA issuers
+  // warps 0-1 weight producers, 2-3 token producers (one of each per stream:
+  // a thread's TMA copies issue one after another, ~150 cycles each, so a
+  // stage's four copies are split over two warps), 4-5 MMA issuers
+  static constexpr int kFirstEpiWarp = 3 * kStreams;
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
   static constexpr int kATile = kBM * kBK;                // unpacked FP4 weight tile (8-bit containers)
   static constexpr int kBTile = kHalf * kBK;
@@ -287,9 +290,17 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   const int total_work = PHASE == 3 ? NT * ((args.MT[0] + args.MT[1]) >> 1) : NT * (args.MT[PHASE - 1] >> 1);
   const int n2_cta_items = 2 * NT * (args.MT[1] >> 1);   // PHASE 3: GEMM2 items x 2 CTAs
 
-  if (warp < C::kStreams) {
+  if (warp < 2 * C::kStreams && (PHASE != 3 || warp < C::kStreams)) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
-    const int st = warp;
+    // Warp st loads the weight part (and arms the stage), warp kStreams + st
+    // the token part of stream st's stages; both pass the same empty
+    // barriers, so a stage one of them issued is issued by the other too (a
+    // wait gives up only on a barrier that has not completed).  The single
+    // launch (PHASE 3) loads whole stages from the weight warp, whose GEMM2
+    // items issue their token part only after the tile's counter wait.
+    const int st = warp % C::kStreams;
+    const bool wpart = PHASE == 3 || warp < C::kStreams;
+    const bool tpart = PHASE == 3 || warp >= C::kStreams;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;
@@ -367,8 +378,8 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
           break;
         }
         if (lane == 0) {
-          issue_weights(gs, kb);
-          issue_tokens(gs, kb);
+          if (wpart) issue_weights(gs, kb);
+          if (tpart) issue_tokens(gs, kb);
         }
         __syncwarp();
         issued_mask |= 1u << gs;
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
     // the leader never leaves with copies in flight (its full barriers count
     // both CTAs' bytes; the other CTA's copies are covered by the final
     // cluster barrier, which the leader reaches only after this drain)
-    if (rank == 0)
+    if (rank == 0 && wpart)
       for (int gs = 0; gs < C::kStages; ++gs)
         if (issued_mask & (1u << gs))
           mbar_wait(&full[gs], (issued_phase >> gs) & 1u, status, kWaitLimit, kWaitProducerDrain, gs, false);
@@ -392,8 +403,10 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
     }
     __syncwarp();
   } else if (warp < 2 * C::kStreams) {
+    // token producer warps of the single launch: idle
+  } else if (warp < 3 * C::kStreams) {
     // ------------------------------------------------------------ MMA issuers (leader only)
-    const int st = warp - C::kStreams;
+    const int st = warp - 2 * C::kStreams;
     if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
