@@ -66,7 +66,7 @@ TRAFFIC = {
     # the CTA-pair kernel (208-token tiles)
     "pair": {
         "sources": PAIR_SOURCES,
-        "src_sha256": "36baa69fe10f4e84f1dbae6e9075efed2e9bc641092c25ef21c5bfb5025b102f",
+        "src_sha256": "6ae5d6f7faba88c3e0c08ce58216480829dde6fc84ec2057da57ccea01687910",
         "prefill": {"gemm1": {"ratio": (533717248 + 8354304) / 511557632, "from": "prefill_e32"},
                     "gemm2": {"ratio": (258542336 + 38179072) / 316932096, "from": "prefill_e32"}},
         "skewed_prefill": {"gemm1": {"ratio": (1195241216 + 33373952) / 1047986176, "from": "skewed_e64"},

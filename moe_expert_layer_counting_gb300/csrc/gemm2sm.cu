@@ -1,27 +1,31 @@
 // gemm2sm.cu -- the expert GEMMs of large problems on CTA pairs: one
-// tcgen05.mma.cta_group::2 (M = 256 weight rows, N up to 224 tokens, K = 32,
+// tcgen05.mma.cta_group::2 (M = 256 weight rows, N up to 208 tokens, K = 32,
 // kind::mxf8f6f4 block-scaled) drives the tensor cores of two SMs.
 //
 // The same GEMM1 (FP8 tokens x FP4 W1|W3, SwiGLU (.) top-k weight, FP8 + UE8M0
 // requantisation) and GEMM2 (FP8 h x FP4 W2 -> BF16 per pair) as gemm.cu, on
-// 224-token tiles.  Prior art: the MMA warp listing of "Warp Specialization:
+// 208-token tiles.  Prior art: the MMA warp listing of "Warp Specialization:
 // DeepEP vs Mega MoE" issues the 2-SM block-scaled MMA from the leader CTA of
 // a pair, and the MegaMoE study notes ("Scheduler") run each tile on a 2-SM
 // cluster.  What a pair buys on GB300:
 //   * each CTA stages its own 128 weight rows but only half of the token rows
-//     (the MMA reads B's halves from both CTAs), so a stage is 31.5 KB instead
-//     of 45.5 KB and five stages fit per SM -- the one-CTA kernel keeps two per
-//     CTA and leaves the tensor pipe waiting on loads;
-//   * one thread issues for two SMs: four MMAs and three scale copies per
-//     128-wide K block keep both tensor cores ~97 % busy at N = 224 (measured
-//     issue rate), and token rows cross L2 -> SM once per pair, not per SM.
-// Roles per CTA (640 threads): warps 0-1 TMA producers of the two issue
-// streams (both CTAs), warps 2-3 their MMA issuers (rank 0 only; warp 2 also
-// allocates TMEM in both CTAs), warps 4-19 epilogue (both CTAs; four column
-// groups of four warps, one TMEM lane quadrant per warp).
+//     (the MMA reads B's halves from both CTAs), so a stage is 30.5 KB instead
+//     of 45.5 KB and six stages fit per SM (three per issue stream) -- the
+//     one-CTA kernel keeps two per CTA and leaves the tensor pipe waiting on
+//     loads;
+//   * one thread issues for two SMs, and two issue streams per pair (each
+//     with its own stages and accumulator) keep the tensor pipes fed while
+//     one stream waits; token rows cross L2 -> SM once per pair, not per SM.
+// Roles per CTA (704 threads): warps 0-1 load the weight part of the two
+// streams' stages (and arm them), warps 2-3 their token part (both CTAs; a
+// thread's TMA copies issue one after another, so a stage's four copies are
+// split over two warps), warps 4-5 the MMA issuers (rank 0 only), warps 6-21
+// the epilogue (both CTAs; four column groups of four warps, one TMEM lane
+// quadrant per warp); warp 2 also initialises the barriers and allocates TMEM.
 // Synchronisation of the pair:
 //   * every load of either CTA counts on the leader's `full` barrier (TMA
-//     .cta_group::2 form); the leader's producer arms it for both CTAs' bytes;
+//     .cta_group::2 form); the leader's weight producer arms it for both
+//     CTAs' bytes;
 //   * the leader's commits arrive on `empty` and `tmem_full` of both CTAs
 //     (multicast); each CTA's epilogue arrives on the leader's `tmem_empty`;
 //   * all waits are bounded (MOE_ERR_TIMEOUT in the status words); the pair
@@ -208,8 +212,8 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   // PHASE 1: GEMM1 + SwiGLU epilogue; 2: GEMM2; 3: expert waves of GEMM1
   // then GEMM2 items in one launch, GEMM2 items waiting on their token
   // tile's arrival counter, then the combine.
-  // A cluster's j-th work item belongs to stream j % 2: producer warp s loads
-  // it into stages [3s, 3s+3), MMA warp 2+s (leader) accumulates it into
+  // A cluster's j-th work item belongs to stream j % 2: producer warps s and
+  // 2+s load it into stages [3s, 3s+3), MMA warp 4+s (leader) accumulates it into
   // accumulator s; the epilogue warps drain the accumulators in item order.
   using C = Pair;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
