@@ -157,7 +157,11 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   if ((fused || pair_layer) && gemms != 0 && gemms != (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2))
     return MOE_ERR_INVALID_ARG;
 
-  if ((phases == 0 || (phases & MOE_PHASE_RESET)) && cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess)
+  // status words and arrival counters zeroed per call: by the front kernel
+  // where it runs (one graph node fewer), otherwise by a memset
+  const bool front_zeroes = phases == 0 && front;
+  if ((phases == 0 || (phases & MOE_PHASE_RESET)) && !front_zeroes &&
+      cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (phases != 0) {
     if (gemms == 0 || a->T == 0) return MOE_OK;
@@ -175,7 +179,8 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   int32_t *inv_perm = reinterpret_cast<int32_t *>(ws + lay.inv_perm);
   if (front_eligible(a->T, a->H, a->E, a->k)) {
     // small problems: routing + permute + pool cast in one launch
-    rc = launch_front(&ea, a->x, a->logits, a->route_mode, idx, wts, inv_perm, ws + lay.expert, st);
+    rc = launch_front(&ea, a->x, a->logits, a->route_mode, idx, wts, inv_perm, ws + lay.expert, status,
+                      (int)(lay.sync_end / 4), st);
     if (rc != MOE_OK) return rc;
     // then, with 16-token tiles, both GEMMs and the combine in one more
     if (fused)

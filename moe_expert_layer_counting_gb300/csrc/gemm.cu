@@ -760,7 +760,7 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts_out,
     int32_t *__restrict__ offsets_out, int32_t *__restrict__ perm_out, int32_t *__restrict__ inv_perm_out,
     uint8_t *__restrict__ chunks, int32_t *__restrict__ tok_pool, float *__restrict__ w_pool,
-    uint2 *__restrict__ xq_pool, int gpc, int mode) {
+    uint2 *__restrict__ xq_pool, int gpc, int mode, int *__restrict__ zero_words, int n_zero) {
   constexpr int kW = kFrontThreads / 32;
   extern __shared__ __align__(16) unsigned char fsm[];
   const int P = T * k;
@@ -782,6 +782,10 @@ __global__ void __launch_bounds__(kFrontThreads) front_kernel(
   const bool writer = blockIdx.x == 0;
   pdl_launch_dependents();
   pdl_wait();
+  // the call's status words and arrival counters (read by the launches after
+  // this one, which wait for its completion)
+  if (writer)
+    for (int i = tid; i < n_zero; i += kFrontThreads) zero_words[i] = 0;
   // 0. this CTA's columns of x (consumed in step 3): the first 16 bytes per
   // thread are loaded into a register here and land in shared memory after
   // routing, so that their latency overlaps the logits loads
@@ -873,7 +877,8 @@ size_t front_smem(int T, int E, int k, int gpc) {
 
 template <int BN>
 int launch_front_t(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
-                   float *wts, int32_t *inv_perm, char *ws, const ExpertWs &lay, cudaStream_t st) {
+                   float *wts, int32_t *inv_perm, char *ws, const ExpertWs &lay, int *zero_words, int n_zero,
+                   cudaStream_t st) {
   // one CTA per 32-value column group of the pool rows, at most two per SM
   const int groups = (int)(a->H / 32);
   const int cap = num_sms() * 2;
@@ -884,7 +889,7 @@ int launch_front_t(const moe_expert_args *a, const uint16_t *x, const float *log
                     const_cast<int32_t *>(a->counts), const_cast<int32_t *>(a->offsets),
                     const_cast<int32_t *>(a->perm), inv_perm, reinterpret_cast<uint8_t *>(ws + lay.sfb1),
                     reinterpret_cast<int32_t *>(ws + lay.tok_pool), reinterpret_cast<float *>(ws + lay.w_pool),
-                    reinterpret_cast<uint2 *>(ws + lay.xq_pool), gpc, mode);
+                    reinterpret_cast<uint2 *>(ws + lay.xq_pool), gpc, mode, zero_words, n_zero);
 }
 
 template <int BN>
@@ -1048,17 +1053,17 @@ bool front_eligible(int64_t T, int64_t H, int E, int k) {
 }
 
 int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
-                 float *wts, int32_t *inv_perm, void *scratch, cudaStream_t st) {
+                 float *wts, int32_t *inv_perm, void *scratch, int *zero_words, int n_zero, cudaStream_t st) {
   const ExpertWs lay = expert_ws_layout(a->T, a->H, a->I, a->E, a->k);
   char *ws = reinterpret_cast<char *>(scratch);
   const int bn = resolve_tile_n(a->tile_n, a->T * a->k, a->E, a->H, a->I);
   switch (bn) {
-    case 16: return launch_front_t<16>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
-    case 32: return launch_front_t<32>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
-    case 64: return launch_front_t<64>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
-    case 128: return launch_front_t<128>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
-    case 208: return launch_front_t<208>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
-    case 224: return launch_front_t<224>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, st);
+    case 16: return launch_front_t<16>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, zero_words, n_zero, st);
+    case 32: return launch_front_t<32>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, zero_words, n_zero, st);
+    case 64: return launch_front_t<64>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, zero_words, n_zero, st);
+    case 128: return launch_front_t<128>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, zero_words, n_zero, st);
+    case 208: return launch_front_t<208>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, zero_words, n_zero, st);
+    case 224: return launch_front_t<224>(a, x, logits, mode, idx, wts, inv_perm, ws, lay, zero_words, n_zero, st);
     default: return MOE_ERR_INVALID_ARG;
   }
 }

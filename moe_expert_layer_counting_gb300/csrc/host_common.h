@@ -121,7 +121,8 @@ int launch_token_cast(const moe_expert_args *a, const uint16_t *x, const int32_t
                       cudaStream_t st);
 // Small problems (front_eligible): routing, counting-sort permute and the pool
 // cast in one launch.  `a` supplies shapes, tile size and the counts / offsets /
-// perm outputs.
+// perm outputs; the kernel also zeroes zero_words[0, n_zero) (the call's status
+// words and arrival counters) before the next launch reads them.
 bool front_eligible(int64_t T, int64_t H, int E, int k);
 // GEMM1 + GEMM2 + combine in one launch after the front kernel (16-token
 // tiles, all CTAs co-resident): eligibility, the arrival counters it needs
@@ -131,7 +132,7 @@ bool fused_eligible(int64_t T, int64_t H, int E, int k, int tile_n);
 size_t fused_sync_ints(int64_t T, int E, int k);
 int launch_fused_gemms(const moe_expert_args *a, uint16_t *y, int *sync, int *status, char *ews, cudaStream_t st);
 int launch_front(const moe_expert_args *a, const uint16_t *x, const float *logits, int mode, int32_t *idx,
-                 float *wts, int32_t *inv_perm, void *scratch, cudaStream_t st);
+                 float *wts, int32_t *inv_perm, void *scratch, int *zero_words, int n_zero, cudaStream_t st);
 // Large problems (224-token tiles): GEMM1 / GEMM2 on 2-CTA clusters sharing
 // one M = 256 MMA (gemm2sm.cu).  Eligible when both GEMMs' 128-row weight
 // tiles pair up (2I/128 and H/128 even) and the shared memory fits.
