@@ -157,10 +157,11 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
   if ((fused || pair_layer) && gemms != 0 && gemms != (MOE_PHASE_GEMM1 | MOE_PHASE_GEMM2))
     return MOE_ERR_INVALID_ARG;
 
-  // status words and arrival counters zeroed per call: by the front kernel
-  // where it runs (one graph node fewer), otherwise by a memset
-  const bool front_zeroes = phases == 0 && front;
-  if ((phases == 0 || (phases & MOE_PHASE_RESET)) && !front_zeroes &&
+  // status words and arrival counters zeroed per call: by the call's first
+  // kernel (the front or the routing kernel; one graph node fewer than a
+  // memset), by a memset when only GEMM launches run (phases) or T = 0
+  const bool kernel_zeroes = phases == 0 && a->T > 0;
+  if ((phases == 0 || (phases & MOE_PHASE_RESET)) && !kernel_zeroes &&
       cudaMemsetAsync(ws, 0, lay.sync_end, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (phases != 0) {
@@ -189,7 +190,7 @@ extern "C" int moe_forward(const moe_forward_args *a, cudaStream_t st) {
     if (rc != MOE_OK) return rc;
     return launch_combine(ea.y_pairs, idx, a->T, a->k, a->H, a->y, st);
   }
-  rc = launch_route(a->logits, a->T, a->E, a->k, a->route_mode, idx, wts, st);
+  rc = launch_route(a->logits, a->T, a->E, a->k, a->route_mode, idx, wts, st, status, (int)(lay.sync_end / 4));
   if (rc != MOE_OK) return rc;
   rc = launch_permute(idx, a->T, a->E, a->k, counts, offsets, perm, inv_perm, status, ws + lay.perm_scratch, st);
   if (rc != MOE_OK) return rc;

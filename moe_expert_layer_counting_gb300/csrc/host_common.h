@@ -105,7 +105,10 @@ inline int choose_tile_n(int64_t P, int64_t E) {
 // Internal launchers (return a moe_status).  `status` points at the two
 // status words of the caller's workspace.
 int launch_quant_act(const uint16_t *x, int64_t rows, int64_t K, uint8_t *q, uint8_t *s, cudaStream_t st);
-int launch_route(const float *logits, int64_t T, int E, int k, int mode, int32_t *idx, float *w, cudaStream_t st);
+// zero_words[0, n_zero) are zeroed too (moe_forward's status words and
+// arrival counters, before the launches that read them)
+int launch_route(const float *logits, int64_t T, int E, int k, int mode, int32_t *idx, float *w, cudaStream_t st,
+                 int *zero_words = nullptr, int n_zero = 0);
 bool route_mode_valid(int mode);
 size_t permute_scratch_bytes(int64_t T, int E, int k);
 int launch_permute(const int32_t *idx, int64_t T, int E, int k, int32_t *counts, int32_t *offsets,

@@ -20,9 +20,14 @@ constexpr int kMaxE = 1024;
 
 __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restrict__ logits, int64_t T, int E,
                                                             int k, int mode, int32_t *__restrict__ idx,
-                                                            float *__restrict__ w) {
+                                                            float *__restrict__ w, int *__restrict__ zero_words,
+                                                            int n_zero) {
   pdl_launch_dependents();
   pdl_wait();
+  // moe_forward: the call's status words and arrival counters (read by the
+  // launches after this one, which wait for its completion)
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < T; t += (int64_t)gridDim.x * kWarps) {
     int my_idx;
@@ -39,12 +44,14 @@ __global__ void __launch_bounds__(kWarps * 32) route_kernel(const float *__restr
 
 }  // namespace
 
-int launch_route(const float *logits, int64_t T, int E, int k, int mode, int32_t *idx, float *w, cudaStream_t st) {
+int launch_route(const float *logits, int64_t T, int E, int k, int mode, int32_t *idx, float *w, cudaStream_t st,
+                 int *zero_words, int n_zero) {
   if (T == 0) return MOE_OK;
   const int64_t blocks = ceil_div(T, kWarps);
   const int64_t cap = (int64_t)num_sms() * 8;
   const int grid = (int)(blocks < cap ? blocks : cap);
-  return launch_pdl(route_kernel, dim3(grid), dim3(kWarps * 32), 0, st, logits, T, E, k, mode, idx, w);
+  return launch_pdl(route_kernel, dim3(grid), dim3(kWarps * 32), 0, st, logits, T, E, k, mode, idx, w, zero_words,
+                    n_zero);
 }
 
 bool route_mode_valid(int mode) {
