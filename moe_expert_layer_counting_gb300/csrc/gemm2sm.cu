@@ -64,7 +64,8 @@ struct Pair {
   static constexpr int kBTile = kHalf * kBK;
   static constexpr int kTokChunk = 1024;                  // token scales of one (tile, K block): 2 x 128 rows
   static constexpr int kSfSlot = 12;                      // TMEM columns per stage: 4 weight + 8 token scales
-  static constexpr int kTmemAcc = kStreams * kBN;         // one accumulator per stream
+  static constexpr int kAccs = 2;                         // accumulators: one per stream, or two for one stream
+  static constexpr int kTmemAcc = kAccs * kBN;
   static constexpr int kTmemCols = kTmemAcc + kSfSlot * kStages;
   // bytes landing on the leader's full barrier per stage (both CTAs; the
   // FP4-unpacking weight load counts its packed bytes)
@@ -76,8 +77,8 @@ struct Pair {
   static constexpr int kOffEpi = kOffSfb + kStages * kTokChunk;
   static constexpr int kOffRow = kOffEpi + 4096 * kEpiGroups;   // y_pairs row [2][BN], weight [2][BN]
   static constexpr int kOffBar = kOffRow + 16 * kBN;
-  // full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], mma_done[2], never
-  static constexpr int kNumBars = 2 * kStages + 3 * kStreams + 1;
+  // full[kStages], empty[kStages], tmem_full[kAccs], tmem_empty[kAccs], mma_done[kStreams], never
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccs + kStreams + 1;
   static constexpr int kOffTmemPtr = (kOffBar + 8 * kNumBars + 63) & ~63;
   static constexpr int kOffScan = kOffTmemPtr + 64;      // block scan: warp sums [0, 32), total [32]
   static constexpr int kOffExp = kOffScan + 256;
@@ -223,8 +224,8 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   uint64_t *full = bars;                         // leader: both CTAs' loads of a stage
   uint64_t *empty = bars + C::kStages;           // each CTA: stage consumed (leader's commit)
   uint64_t *tmem_full = bars + 2 * C::kStages;   // each CTA: accumulator s ready (leader's commit)
-  uint64_t *tmem_empty = tmem_full + C::kStreams;  // leader: both CTAs' epilogues drained accumulator s
-  uint64_t *mma_done = tmem_empty + C::kStreams;
+  uint64_t *tmem_empty = tmem_full + C::kAccs;    // leader: both CTAs' epilogues drained accumulator a
+  uint64_t *mma_done = tmem_empty + C::kAccs;     // per stream
   uint64_t *never = mma_done + C::kStreams;
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + C::kOffTmemPtr);
   int *vote = reinterpret_cast<int *>(smem + C::kOffTmemPtr + 4);
@@ -267,9 +268,11 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], 1);
       }
-      for (int a = 0; a < C::kStreams; ++a) {
+      for (int a = 0; a < C::kAccs; ++a) {
         mbar_init(&tmem_full[a], 1);
         mbar_init(&tmem_empty[a], 2 * C::kEpiWarps);
+      }
+      for (int a = 0; a < C::kStreams; ++a) {
         mbar_init(&mma_done[a], 1);
       }
       mbar_init(never, 1);
@@ -414,15 +417,18 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
     if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t d_tmem = tmem_base + (uint32_t)(st * C::kBN);
-      for (int w = cluster + st * nclusters; w < total_work && ok; w += C::kStreams * nclusters) {
+      int jj = 0;                                  // this stream's item count
+      for (int w = cluster + st * nclusters; w < total_work && ok; w += C::kStreams * nclusters, ++jj) {
         const PairItem it = decode_pair_item<PHASE>(w, args, NT, tile_off, cnt_sm, off_sm);
         const int KB = args.KB[it.gemm];
         const uint32_t n_mma = (uint32_t)min(C::kBN, (it.ti.valid + 31) & ~31);
-        if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(2, mbar_wait(&tmem_empty[st], acc_phase ^ 1, status, kWaitLimit,
-                                                                 kWaitMmaTmemEmpty, w))))
+        // the accumulator: the stream's own (two streams), or alternating (one)
+        const int acc = C::kStreams == 1 ? (jj & 1) : st;
+        const uint32_t acc_use = C::kStreams == 1 ? (uint32_t)(jj >> 1) : (uint32_t)jj;   // earlier uses of it
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kBN);
+        if (!__all_sync(0xffffffffu, MXQ_TIMED_WAIT(2, mbar_wait(&tmem_empty[acc], (acc_use & 1u) ^ 1u, status,
+                                                                 kWaitLimit, kWaitMmaTmemEmpty, w))))
           break;
         if (args.inject_wait == 1 && w == cluster + st * nclusters &&
             !__all_sync(0xffffffffu, mbar_wait(never, 0, status, kInjectedWaitLimit, kWaitInjected, w)))
@@ -465,9 +471,8 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
           if (++stage == C::kStagesPerStream) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        if (elect_one()) tc_commit_2sm(&tmem_full[st], 3);
+        if (elect_one()) tc_commit_2sm(&tmem_full[acc], 3);
         __syncwarp();
-        acc_phase ^= 1;
       }
       // every MMA of this thread completes before the pair frees TMEM
       if (lane == 0) tc_commit_2sm(&mma_done[st], 1);
