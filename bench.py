@@ -66,24 +66,24 @@ TRAFFIC = {
     # the CTA-pair kernel (208-token tiles)
     "pair": {
         "sources": PAIR_SOURCES,
-        "src_sha256": "6ae5d6f7faba88c3e0c08ce58216480829dde6fc84ec2057da57ccea01687910",
-        "prefill": {"gemm1": {"ratio": (533717248 + 8354304) / 511557632, "from": "prefill_e32"},
-                    "gemm2": {"ratio": (258542336 + 38179072) / 316932096, "from": "prefill_e32"}},
-        "skewed_prefill": {"gemm1": {"ratio": (1195241216 + 33373952) / 1047986176, "from": "skewed_e64"},
-                           "gemm2": {"ratio": (535361536 + 196535296) / 768606208, "from": "skewed_e64"}},
+        "src_sha256": "8e31820fc88419f7b3dc8c286e777d0fd18c8cc0f4796fcf9955f3353bc5555f",
+        "prefill": {"gemm1": {"ratio": (533808896 + 8546304) / 511557632, "from": "prefill_e32"},
+                    "gemm2": {"ratio": (258586112 + 38180096) / 316932096, "from": "prefill_e32"}},
+        "skewed_prefill": {"gemm1": {"ratio": (1190588672 + 33292288) / 1047986176, "from": "skewed_e64"},
+                           "gemm2": {"ratio": (535838976 + 195479552) / 768606208, "from": "skewed_e64"}},
     },
     # the one-CTA kernel (small tiles; the small decode's fused launch)
     "one_cta": {
         "sources": ONE_CTA_SOURCES,
-        "src_sha256": "b6b740adc635142926e2264a069ebd6c3414e6ac6a7d398d145f86f1a4f9a042",
-        "small_decode": {"fused": {"bytes": 94067200 + 1632512, "from": "small_decode (full size)"}},
+        "src_sha256": "00bb534b5938cedf0335fbbd77d700aa126883961cdaf1ab36e8a59c9fa53683",
+        "small_decode": {"fused": {"bytes": 94067968 + 1623040, "from": "small_decode (full size)"}},
     },
 }
 # the same for the block-FP8 variant's GEMMs (csrc/bfp8.cu)
 BFP8_SOURCES = ("bfp8.cu", "ptx.cuh", "layer_blocks.cuh", "host_common.h")
 TRAFFIC_BFP8 = {
-    "src_sha256": "29ff1ef0a0028b43fb3a4f0da822dcb433f7974b4f09276cbad094a1457b5186",
-    "small_decode": {"gemm1": 117679360 + 427264, "gemm2": 58838272 + 57088},
+    "src_sha256": "79311228cdde91d3cbb71523b34469c098f4a6b51a34adabb51fdec33e737862",
+    "small_decode": {"gemm1": 117678592 + 65280, "gemm2": 58821888 + 25856},
 }
 UNIT = "tokens/s"
 
