@@ -66,3 +66,21 @@ def test_layer_rates():
     r = bench.layer_rates(alg, 0.0394)                 # 39.4 us per step
     assert r["gbs"] == round(94e6 / 39.4e-6 / 1e9, 1)
     assert r["tflops"] == round(402653184 / 39.4e-6 / 1e12, 3)
+
+
+def test_traffic_table_lookup():
+    # every kernel family names existing sources and a SHA-256; a workload or
+    # launch without a capture reads as "not captured", a captured one gives
+    # bytes (while its sources still hash to the recorded value) or says why not
+    for fam in bench.TRAFFIC.values():
+        assert len(fam["src_sha256"]) == 64
+        assert bench.gemm_sources_sha256(fam["sources"])
+    assert bench.measured_traffic("tiny", "fused", 1000) == (None, "not captured")
+    assert bench.measured_traffic("large_decode", "gemm1", 1000) == (None, "not captured")
+    fresh = bench.gemm_sources_sha256(bench.PAIR_SOURCES) == bench.TRAFFIC["pair"]["src_sha256"]
+    nbytes, how = bench.measured_traffic("prefill", "gemm1", 10**9)
+    if fresh:
+        ratio = bench.TRAFFIC["pair"]["prefill"]["gemm1"]["ratio"]
+        assert nbytes == round(ratio * 10**9) and "prefill_e32" in how
+    else:
+        assert nbytes is None and "changed" in how
