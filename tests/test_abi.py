@@ -87,6 +87,16 @@ def test_host_validation_rejects_bad_arguments():
     f.T, f.H, f.I, f.E, f.k = 8, 256, 128, 4, 2
     f.workspace, f.workspace_bytes = 0x1000, 100
     assert L.moe_forward(ctypes.byref(f), s0) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    for bad_phases in (32, 1, 8):                     # unknown bit; TOKEN_SCALES / H_SCALES are not forward phases
+        f.phases = bad_phases
+        assert L.moe_forward(ctypes.byref(f), s0) == B.MOE_ERR_INVALID_ARG
+    f.phases = 0
+    for bad_schedule in (-1, 3):
+        f.schedule = bad_schedule
+        assert L.moe_forward(ctypes.byref(f), s0) == B.MOE_ERR_INVALID_ARG
+    f.schedule = B.SCHEDULE_EXPERT_WAVES
+    f.workspace = 0x1080                              # not 256-byte aligned
+    assert L.moe_forward(ctypes.byref(f), s0) == B.MOE_ERR_MISALIGNED
     assert B.moe_status_string(B.MOE_ERR_TIMEOUT).startswith("a device-side wait")
 
 
