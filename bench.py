@@ -66,11 +66,11 @@ TRAFFIC = {
     # the CTA-pair kernel (208-token tiles)
     "pair": {
         "sources": PAIR_SOURCES,
-        "src_sha256": "8e31820fc88419f7b3dc8c286e777d0fd18c8cc0f4796fcf9955f3353bc5555f",
-        "prefill": {"gemm1": {"ratio": (533808896 + 8546304) / 511557632, "from": "prefill_e32"},
-                    "gemm2": {"ratio": (258586112 + 38180096) / 316932096, "from": "prefill_e32"}},
-        "skewed_prefill": {"gemm1": {"ratio": (1190588672 + 33292288) / 1047986176, "from": "skewed_e64"},
-                           "gemm2": {"ratio": (535838976 + 195479552) / 768606208, "from": "skewed_e64"}},
+        "src_sha256": "06266b645b27a68e982d192fe8a19bf1f49d5f3aeaba799c6f018472937ddf9d",
+        "prefill": {"gemm1": {"ratio": (533650944 + 8379392) / 511557632, "from": "prefill_e32"},
+                    "gemm2": {"ratio": (258542592 + 38111744) / 316932096, "from": "prefill_e32"}},
+        "skewed_prefill": {"gemm1": {"ratio": (1188315136 + 33220864) / 1047986176, "from": "skewed_e64"},
+                           "gemm2": {"ratio": (535210240 + 196240896) / 768606208, "from": "skewed_e64"}},
     },
     # the one-CTA kernel (small tiles; the small decode's fused launch)
     "one_cta": {

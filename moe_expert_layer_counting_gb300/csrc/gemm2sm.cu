@@ -16,12 +16,13 @@
 //   * one thread issues for two SMs, and two issue streams per pair (each
 //     with its own stages and accumulator) keep the tensor pipes fed while
 //     one stream waits; token rows cross L2 -> SM once per pair, not per SM.
-// Roles per CTA (704 threads): warps 0-1 load the weight part of the two
-// streams' stages (and arm them), warps 2-3 their token part (both CTAs; a
-// thread's TMA copies issue one after another, so a stage's four copies are
-// split over two warps), warps 4-5 the MMA issuers (rank 0 only), warps 6-21
-// the epilogue (both CTAs; four column groups of four warps, one TMEM lane
-// quadrant per warp); warp 2 also initialises the barriers and allocates TMEM.
+// Roles per CTA (768 threads): warps 0-1 load the weight codes of the two
+// streams' stages (and arm them), warps 2-3 their token rows, warps 4-5 both
+// scale parts (both CTAs; a thread's TMA copies issue one after another, so
+// a stage's copies are spread over three warps), warps 6-7 the MMA issuers
+// (rank 0 only), warps 8-23 the epilogue (both CTAs; four column groups of
+// four warps, one TMEM lane quadrant per warp); warp 2 also initialises the
+// barriers and allocates TMEM.
 // Synchronisation of the pair:
 //   * every load of either CTA counts on the leader's `full` barrier (TMA
 //     .cta_group::2 form); the leader's weight producer arms it for both
@@ -55,10 +56,11 @@ struct Pair {
   static constexpr int kStages = kStreams * kStagesPerStream;
   static constexpr int kEpiWarps = 16;                    // four groups of four (one TMEM lane quadrant each)
   static constexpr int kEpiGroups = kEpiWarps / 4;
-  // warps 0-1 weight producers, 2-3 token producers (one of each per stream:
-  // a thread's TMA copies issue one after another, ~150 cycles each, so a
-  // stage's four copies are split over two warps), 4-5 MMA issuers
-  static constexpr int kFirstEpiWarp = 3 * kStreams;
+  // warps 0-1 weight-code producers, 2-3 token-row producers, 4-5 scale
+  // producers (one of each per stream: a thread's TMA copies issue one after
+  // another, ~150 cycles each, so a stage's copies are spread over three
+  // warps), 6-7 MMA issuers
+  static constexpr int kFirstEpiWarp = 4 * kStreams;
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
   static constexpr int kATile = kBM * kBK;                // unpacked FP4 weight tile (8-bit containers)
   static constexpr int kBTile = kHalf * kBK;
@@ -213,8 +215,8 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   // PHASE 1: GEMM1 + SwiGLU epilogue; 2: GEMM2; 3: expert waves of GEMM1
   // then GEMM2 items in one launch, GEMM2 items waiting on their token
   // tile's arrival counter, then the combine.
-  // A cluster's j-th work item belongs to stream j % 2: producer warps s and
-  // 2+s load it into stages [3s, 3s+3), MMA warp 4+s (leader) accumulates it into
+  // A cluster's j-th work item belongs to stream j % 2: producer warps s, 2+s
+  // and 4+s load it into stages [3s, 3s+3), MMA warp 6+s (leader) accumulates it into
   // accumulator s; the epilogue warps drain the accumulators in item order.
   using C = Pair;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -297,17 +299,20 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
   const int total_work = PHASE == 3 ? NT * ((args.MT[0] + args.MT[1]) >> 1) : NT * (args.MT[PHASE - 1] >> 1);
   const int n2_cta_items = 2 * NT * (args.MT[1] >> 1);   // PHASE 3: GEMM2 items x 2 CTAs
 
-  if (warp < 2 * C::kStreams && (PHASE != 3 || warp < C::kStreams)) {
+  if (warp < 3 * C::kStreams && (PHASE != 3 || warp < C::kStreams)) {
     // ------------------------------------------------------------ TMA producers (both CTAs)
-    // Warp st loads the weight part (and arms the stage), warp kStreams + st
-    // the token part of stream st's stages; both pass the same empty
-    // barriers, so a stage one of them issued is issued by the other too (a
-    // wait gives up only on a barrier that has not completed).  The single
-    // launch (PHASE 3) loads whole stages from the weight warp, whose GEMM2
-    // items issue their token part only after the tile's counter wait.
+    // Warp st loads the weight codes (and arms the stage), warp kStreams + st
+    // the token rows and warp 2 kStreams + st both scale parts of stream st's
+    // stages; all pass the same empty barriers, so a stage one of them issued
+    // is issued by the others too (a wait gives up only on a barrier that has
+    // not completed).  The single launch (PHASE 3) loads whole stages from the
+    // weight warp, whose GEMM2 items issue their token part only after the
+    // tile's counter wait.
     const int st = warp % C::kStreams;
-    const bool wpart = PHASE == 3 || warp < C::kStreams;
-    const bool tpart = PHASE == 3 || warp >= C::kStreams;
+    const int role = warp / C::kStreams;         // 0: weight codes (arms), 1: token rows, 2: both scale parts
+    const bool wpart = PHASE == 3 || role == 0;
+    const bool tpart = PHASE == 3 || role == 1;
+    const bool spart = PHASE == 3 || role == 2;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_phase = 0;
@@ -385,8 +390,19 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
           break;
         }
         if (lane == 0) {
-          if (wpart) issue_weights(gs, kb);
-          if (tpart) issue_tokens(gs, kb);
+          const uint32_t bar = mapa_shared(smem_u32(&full[gs]), 0);
+          if (wpart) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[gs], C::kStageTx);
+            tma_load_2d_2sm(smem + C::kOffA + gs * C::kATile, tw, bar, 0, (wtile + kb) * kBM);
+            if (kb + kPrefetchAhead < KB)
+              prefetch_l2_bulk(args.w_codes[gm] + ((size_t)wtile + kb + kPrefetchAhead) * kWTileBytes, kWTileBytes);
+          }
+          if (tpart)
+            tma_load_2d_2sm(smem + C::kOffB + gs * C::kBTile, tb, bar, kb * kBK, ti.s0 + (int)rank * (n_mma >> 1));
+          if (spart) {
+            tma_load_2d_2sm(smem + C::kOffSfa + gs * 512, twsf, bar, 0, (wtile + kb) * 2);
+            tma_load_2d_2sm(smem + C::kOffSfb + gs * C::kTokChunk, tbsf, bar, 0, (ti.g * KB + kb) * 4);
+          }
         }
         __syncwarp();
         issued_mask |= 1u << gs;
@@ -409,11 +425,11 @@ __global__ void __launch_bounds__(Pair::kThreads, 1)
       while (clock64() - t0 < 200000) __nanosleep(1000);
     }
     __syncwarp();
-  } else if (warp < 2 * C::kStreams) {
-    // token producer warps of the single launch: idle
   } else if (warp < 3 * C::kStreams) {
+    // token / scale producer warps of the single launch: idle
+  } else if (warp < 4 * C::kStreams) {
     // ------------------------------------------------------------ MMA issuers (leader only)
-    const int st = warp - 2 * C::kStreams;
+    const int st = warp - 3 * C::kStreams;
     if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
